@@ -1,0 +1,220 @@
+"""FP8 E4M3 per-128 group quant with packed UE8M0 scales, and the einsum
+that consumes them.  Written from definitions.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+[PR] "implementation breakdown" item 1 and the "key source snippets"
+section fix the producer: for every token t, outer group g and 128-wide
+hidden group j of x[T, G, D], an absmax -> UE8M0 exponent byte is written
+into an int32 pack; pack index j // 4, byte j % 4; physical layout
+[G, ceil((D/128)/4), align_up(T, 4)] with the token dimension contiguous;
+the bytes of the last pack past the last hidden group are zeroed.
+Item 2 (the Python wrapper) fixes the storage sizes and the logical view
+[T, G, P] with strides (1, P*Ta, Ta).  The scale rule
+s = 2**ceil(log2(absmax / 448)) and round-to-nearest-even satfinite E4M3
+payloads are the readings used (the digest prints neither).
+
+Readings for silent points:
+  * absmax == 0 gives exponent -127 (byte 0); exponents are clamped to
+    [-127, 127];
+  * token-padding words t in [T, Ta) are written as zero (the page leaves
+    them uninitialised and hides them by slicing);
+  * D must be a multiple of 128.
+"""
+import math
+
+import numpy as np
+
+from .codecs import bf16_to_f32, e4m3_encode, e4m3_decode, ue8m0_decode
+
+GROUP = 128          # hidden elements per scale group
+PACK = 4             # UE8M0 bytes per int32 pack ([PR] UE8M0_SCALES_PER_PACK)
+E4M3_MAX = 448.0
+
+
+def packed_dims(T, D):
+    """(NG, P, Ta): hidden groups, packs per row, token count aligned up to 4."""
+    if D % GROUP:
+        raise ValueError("D must be a multiple of 128")
+    NG = D // GROUP
+    P = (NG + PACK - 1) // PACK
+    Ta = (T + PACK - 1) // PACK * PACK
+    return NG, P, Ta
+
+
+def ue8m0_exponent(amax):
+    """e = ceil(log2(amax / 448)) clamped to [-127, 127]; amax == 0 -> -127.
+
+    amax is a bf16 value, so amax / 448 in float64 is the exact quotient
+    rounded once and cannot cross a power of two (448 = 7 * 2**6 and amax
+    has 8 significant bits); frexp then gives the exponent exactly:
+    r = m * 2**ex with 0.5 <= m < 1, so ceil(log2 r) = ex, or ex - 1 when
+    m == 0.5 (r is a power of two).
+    """
+    a = float(amax)
+    if a == 0.0:
+        return -127
+    m, ex = math.frexp(a / E4M3_MAX)
+    e = ex - 1 if m == 0.5 else ex
+    return max(-127, min(127, e))
+
+
+def quant_fp8_group(x_bf16):
+    """Per-(t, g, 128-group) FP8 quant.  x bf16 bits [T, G, D].
+
+    Returns (xq uint8 E4M3 codes [T, G, D], e int32 exponents [T, G, NG]).
+    q = E4M3_RN_satfinite(x * 2**-e); x * 2**-e is exact in float64.
+    """
+    x = bf16_to_f32(np.asarray(x_bf16, np.uint16)).astype(np.float64)
+    T, G, D = x.shape
+    NG, _, _ = packed_dims(T, D)
+    xg = x.reshape(T, G, NG, GROUP)
+    amax = np.max(np.abs(xg), axis=3) if T else np.zeros((0, G, NG))
+    e = np.vectorize(ue8m0_exponent, otypes=[np.int64])(amax) if amax.size else \
+        np.zeros(amax.shape, np.int64)
+    scaled = xg * np.ldexp(1.0, -e)[..., None]
+    xq = e4m3_encode(scaled).reshape(T, G, D)
+    return xq, e.astype(np.int32)
+
+
+def pack_exponents(e, T, G, NG):
+    """Place UE8M0 bytes u = e + 127 into the packed [G, P, Ta] int32 layout.
+
+    Byte (t, g, j) sits at byte offset ((g*P + j//4)*Ta + t)*4 + j%4 of a
+    zero-initialised little-endian int32 buffer, which leaves the unused
+    bytes of the last pack and the token-padding words at zero.
+    [PR] key source snippets (word offset (outer*P + pack)*Ta + token, byte
+    offset pack_byte_idx) and implementation breakdown item 1 (tail zeroing).
+    """
+    P = (NG + PACK - 1) // PACK
+    Ta = (T + PACK - 1) // PACK * PACK
+    buf = np.zeros(G * P * Ta * PACK, dtype=np.uint8)
+    for t in range(T):
+        for g in range(G):
+            for j in range(NG):
+                off = ((g * P + j // PACK) * Ta + t) * PACK + j % PACK
+                buf[off] = np.uint8(int(e[t, g, j]) + 127)
+    return buf.view("<i4").reshape(G, P, Ta).astype(np.int32)
+
+
+def quant_fp8_group_ue8m0_packed(x_bf16):
+    """The producer: E4M3 payload + packed UE8M0 scale storage [G, P, Ta] int32."""
+    x = np.asarray(x_bf16, np.uint16)
+    T, G, D = x.shape
+    NG, _, _ = packed_dims(T, D)
+    xq, e = quant_fp8_group(x)
+    return xq, pack_exponents(e, T, G, NG)
+
+
+def quant_fp8_group_fp32_scales(x_bf16):
+    """Producer with unpacked scales: E4M3 payload + fp32 [T, G, NG] holding 2**e.
+
+    This is the pre-PR form ([PR] motivation: the quant still emitted fp32
+    activation scales and a separate repack ran before every einsum).
+    """
+    xq, e = quant_fp8_group(x_bf16)
+    return xq, np.ldexp(np.float32(1.0), e).astype(np.float32)
+
+
+def logical_scale_view(storage, T):
+    """Logical [T, G, P] view of the [G, P, Ta] storage, strides (1, P*Ta, Ta).
+
+    [PR] implementation breakdown item 2: transpose(-1, -2), slice the token
+    padding, transpose(0, 1).
+    """
+    return np.asarray(storage).transpose(0, 2, 1)[:, :T, :].transpose(1, 0, 2)
+
+
+def repack_fp32_scales_to_ue8m0(sx_f32):
+    """fp32 power-of-two scales [T, G, NG] -> packed UE8M0 int32 [G, P, Ta].
+
+    The separate conversion the PR removed ([PR] motivation,
+    transpose_and_pack_fp32_into_ue8m0).  Written independently of
+    pack_exponents: each scale's exponent is read with frexp (a power of two
+    2**e has frexp mantissa 0.5 and exponent e + 1), and the word for
+    (g, pack, t) is assembled from its four bytes, zero where j >= NG.
+    """
+    s = np.asarray(sx_f32, np.float32)
+    T, G, NG = s.shape
+    P = (NG + PACK - 1) // PACK
+    Ta = (T + PACK - 1) // PACK * PACK
+    out = np.zeros((G, P, Ta), dtype=np.int64)
+    for g in range(G):
+        for p in range(P):
+            for t in range(T):
+                word = 0
+                for b in range(PACK):
+                    j = p * PACK + b
+                    if j >= NG:
+                        continue
+                    m, ex = math.frexp(float(s[t, g, j]))
+                    if m != 0.5:
+                        raise ValueError("scale is not a power of two")
+                    word |= ((ex - 1) + 127) << (8 * b)
+                out[g, p, t] = word
+    return out.astype(np.uint32).view(np.int32)
+
+
+def unpack_scales(storage, T, NG):
+    """Packed [G, P, Ta] int32 -> float64 scales [T, G, NG] (2**(u-127))."""
+    st = np.ascontiguousarray(np.asarray(storage, np.int32))
+    G, P, Ta = st.shape
+    by = st.view(np.uint8).reshape(G, P, Ta, PACK)
+    u = np.zeros((T, G, NG), np.uint8)
+    for j in range(NG):
+        u[:, :, j] = by[:, j // PACK, :T, j % PACK].T
+    return ue8m0_decode(u)
+
+
+def quantize_weight_fp8_block(w_gnd):
+    """Offline weight prep: fp32 W stored [G, N, D] (logical W[g, d, n]).
+
+    For each 128 x 128 block (d-block kb, n-block nb):
+    sw = fp32(amax / 448) and wq = E4M3_RN_satfinite(fp32(w / sw)), both
+    fp32 divisions; an all-zero block gives sw = 0 and codes 0.
+    Returns (wq uint8 [G, N, D], sw fp32 [G, D/128, N/128]).
+    Reading: the plain per-block absmax scheme for "fp32 per-128x128 block
+    scales" (the pages name the consumer, DeepGEMM fp8_einsum, but not its
+    weight recipe).
+    """
+    w = np.asarray(w_gnd, np.float32)
+    G, N, D = w.shape
+    if D % GROUP or N % GROUP:
+        raise ValueError("N and D must be multiples of 128")
+    wb = w.reshape(G, N // GROUP, GROUP, D // GROUP, GROUP)        # g, nb, n, kb, d
+    amax = np.max(np.abs(wb), axis=(2, 4))                           # [G, NB, KB]
+    sw = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (wb / sw[:, :, None, :, None]).astype(np.float32)
+    r = np.where(np.isnan(r), np.float32(0), r)
+    wq = e4m3_encode(r).reshape(G, N, D)
+    return wq, np.ascontiguousarray(sw.transpose(0, 2, 1))           # [G, KB, NB]
+
+
+def fp8_group_einsum(xq, sx, wq_gnd, sw_blk):
+    """Y[t, g, n] = bf16( sum_kb sx[t,g,kb] * sw[g,kb,n/128] * sum_{d in kb} xq*wq ).
+
+    xq uint8 E4M3 [T, G, D]; sx float [T, G, NG] (decoded scales, from either
+    the packed or the fp32 format); wq uint8 E4M3 [G, N, D]; sw fp32
+    [G, D/128, N/128].  Each 128-term block sum of E4M3 products is exact in
+    float64 (products are multiples of 2**-18 below 2**18); the scaled blocks
+    are summed in float64 and the result is rounded ONCE to bf16.
+    [PR] the consumer deep_gemm.fp8_einsum reading the packed activation
+    scales (motivation; implementation breakdown item 3).
+    """
+    from .codecs import f64_to_bf16
+    xv = e4m3_decode(xq)
+    wv = e4m3_decode(wq_gnd)
+    T, G, D = xv.shape
+    N = wv.shape[1]
+    KB = D // GROUP
+    y = np.zeros((T, G, N), np.float64)
+    sx = np.asarray(sx, np.float64)
+    sw = np.asarray(sw_blk, np.float32).astype(np.float64)
+    for g in range(G):
+        for kb in range(KB):
+            d0 = kb * GROUP
+            blk = xv[:, g, d0:d0 + GROUP] @ wv[g, :, d0:d0 + GROUP].T       # [T, N], exact
+            swn = np.repeat(sw[g, kb, :], GROUP)                             # per n
+            y[:, g, :] += blk * sx[:, g, kb][:, None] * swn[None, :]
+    return f64_to_bf16(y)
