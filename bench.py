@@ -1,0 +1,626 @@
+#!/usr/bin/env python
+"""Benchmark of the decode quant + quantized-linear path (one JSON line).
+
+Headline workload - the INT8 W8A8 M-sweep on two DeepSeek-V4 linears:
+(K=4096, N=1024) and (K=1024, N=32768), M in {1,2,3,4,7,8,9,16,32,64};
+X bf16 ~ N(0,1) with 0.1% x50 outliers, W int8 uniform [-127,127], per-channel
+scales U[1e-3,1e-2].  One step = for every (linear, M): the standalone
+per-token quant, the standalone W8A8 GEMM on its output, and the fused
+quant + GEMM.  Throughput = algorithmic bytes of the step / step time (GB/s).
+
+Timing: device-resident inputs, each op group captured once as a CUDA graph
+and replayed; CUDA events on the launching stream; W warm-up steps, then K
+timed steps between a barrier + synchronize.  Every call reads its own copy
+of the weights and a step reads 720 MB of weights (> 2x the 129 MB L2), so
+each call streams its weights from HBM.  Activations stay L2-hot, as they
+would right after the producing kernel in a decode step.
+
+Also reported: per-call microseconds and GB/s for every (op, linear, M); the
+other workloads (FP8 group quant with packed UE8M0 scales, the block-scaled
+einsum in both scale formats, the fp32-scale + repack control, the MoE
+expert chain); an end-to-end number through the public API with host
+buffers; the roofline of the dominant kernel; the CPU oracle on the host's
+cores; SM clocks sampled during the timed region.
+
+`--impl reference` times the CPU oracle (the reference arm) on the same
+workload, metric and unit.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/call & GB/s per quantized linear vs M=1..64; % of GB300 HBM/tensor peak"
+UNIT = "GB/s"
+MS = [1, 2, 3, 4, 7, 8, 9, 16, 32, 64]
+LINEARS = [(4096, 1024), (1024, 32768)]
+SEED = 0x5EED0000
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def bytes_quant(M, K):
+    return 2 * M * K + M * K + 4 * M
+
+
+def bytes_gemm(M, K, N):
+    return N * K + 4 * N + M * K + 4 * M + 2 * M * N
+
+
+def bytes_fused(M, K, N):
+    return N * K + 4 * N + 2 * M * K + 2 * M * N
+
+
+def step_bytes():
+    return sum(bytes_quant(M, K) + bytes_gemm(M, K, N) + bytes_fused(M, K, N) for K, N in LINEARS for M in MS)
+
+
+def bytes_group_quant(T, G, D):
+    Ta = (T + 3) // 4 * 4
+    return 2 * T * G * D + T * G * D + 4 * G * ((D // 128 + 3) // 4) * Ta
+
+
+def bytes_einsum(T, G, D, N):
+    Ta = (T + 3) // 4 * 4
+    P = (D // 128 + 3) // 4
+    return G * D * N + 4 * G * (D // 128) * (N // 128) + T * G * D + 4 * G * P * Ta + 2 * T * G * N
+
+
+# ---------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def traffic_for(kernel_key, sources):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    h = hashlib.sha256()
+    for s in sources:
+        h.update(open(os.path.join(ROOT, s), "rb").read())
+    return d["dram_bytes_per_launch"] if d.get("source_sha256") == h.hexdigest() else None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [l for (t, l) in self.lines if t0 <= t <= t1 + 0.15]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        if not rows:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the fq arm
+def run_fq(args, rank, world, local_rank):
+    import torch
+    import fp8_dynamic_quant_gb300 as fq
+    from fp8_dynamic_quant_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    fq.lib()  # fail loudly if the library is missing
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+
+    def bf(a):
+        import numpy as np
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    # ---------------- headline workload buffers
+    n_copies = {}
+    W, SW = {}, {}
+    for (K, N) in LINEARS:
+        wbytes = K * N
+        n_copies[(K, N)] = max(20, -(-2 * l2 // wbytes) + 1)
+        W[(K, N)] = [synth.uniform_int8_device((N, K), SEED + 100 * i + K + N, dev) for i in range(n_copies[(K, N)])]
+        SW[(K, N)] = [synth.uniform_f32_device((N,), 1e-3, 1e-2, SEED + 7 + 100 * i + N, dev)
+                      for i in range(n_copies[(K, N)])]
+    X, XQ, SX, Y, YF = {}, {}, {}, {}, {}
+    for (K, N) in LINEARS:
+        for M in MS:
+            X[(K, N, M)] = bf(synth.activations(M, K, SEED + 1000 + M + K))
+            XQ[(K, N, M)] = torch.empty((M, K), dtype=torch.int8, device=dev)
+            SX[(K, N, M)] = torch.empty((M,), dtype=torch.float32, device=dev)
+            Y[(K, N, M)] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            YF[(K, N, M)] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws_bytes = max(fq.workspace_bytes(fq.OP_W8A8_QUANT_LINEAR, 64, K, N) for (K, N) in LINEARS)
+    ws_bytes = max(ws_bytes, fq.workspace_bytes(fq.OP_FP8_GROUP_EINSUM, 256, 4096, 1024, 8))
+    ws = fq.new_workspace(ws_bytes, dev)
+
+    def call_quant(K, N, M):
+        fq.dynamic_quant_int8(X[(K, N, M)], XQ[(K, N, M)], SX[(K, N, M)])
+
+    def call_gemm(K, N, M, c):
+        fq.w8a8_linear(XQ[(K, N, M)], SX[(K, N, M)], W[(K, N)][c], SW[(K, N)][c], y=Y[(K, N, M)], ws=ws)
+
+    def call_fused(K, N, M, c):
+        fq.w8a8_quant_linear(X[(K, N, M)], W[(K, N)][c], SW[(K, N)][c], y=YF[(K, N, M)], ws=ws)
+
+    small, big = LINEARS
+    groups = [
+        ("quant", lambda: [call_quant(K, N, M) for (K, N) in LINEARS for M in MS],
+         sum(bytes_quant(M, K) for (K, N) in LINEARS for M in MS), 2 * len(MS)),
+        ("gemm_K4096_N1024", lambda: [call_gemm(*small, M, i) for i, M in enumerate(MS)],
+         sum(bytes_gemm(M, *small) for M in MS), len(MS)),
+        ("gemm_K1024_N32768", lambda: [call_gemm(*big, M, i) for i, M in enumerate(MS)],
+         sum(bytes_gemm(M, *big) for M in MS), len(MS)),
+        ("fused_K4096_N1024", lambda: [call_fused(*small, M, 10 + i) for i, M in enumerate(MS)],
+         sum(bytes_fused(M, *small) for M in MS), 2 * len(MS)),
+        ("fused_K1024_N32768", lambda: [call_fused(*big, M, 10 + i) for i, M in enumerate(MS)],
+         sum(bytes_fused(M, *big) for M in MS), 2 * len(MS)),
+    ]
+    launches_per_step = sum(g[3] for g in groups)
+
+    # eager warm-up of every call (lazy host-side set-up), then capture
+    for _, fn, _, _ in groups:
+        fn()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(dev)
+    graphs = []
+    for name, fn, nbytes, nl in groups:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        graphs.append((name, g, nbytes, nl))
+    torch.cuda.synchronize()
+
+    def step(evs=None):
+        for i, (_, g, _, _) in enumerate(graphs):
+            if evs is not None:
+                evs[i].record()
+            g.replay()
+        if evs is not None:
+            evs[len(graphs)].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+    K_steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(K_steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_start.record()
+    for k in range(K_steps):
+        step(evs[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    time.sleep(0.15)
+    clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    group_ms = [sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K_steps)) / K_steps for i in range(len(graphs))]
+    ms_per_step = total_ms / K_steps
+    sb = step_bytes()
+    value = world * sb / (ms_per_step * 1e-3) / 1e9
+
+    group_report = {}
+    for (name, _, nbytes, nl), ms in zip(graphs, group_ms):
+        gbps = nbytes / (ms * 1e-3) / 1e9
+        group_report[name] = {"us_per_step": round(ms * 1e3, 2), "launches": nl, "GBps": round(gbps, 1),
+                              "frac_hbm": round(gbps / hbm_peak, 3)}
+
+    # roofline of the dominant kernel: the W8A8 GEMM on the (K=1024, N=32768) linear
+    dom_ms = group_ms[2]
+    dom_bytes_per_launch = groups[2][2] / len(MS)
+    achieved = dom_bytes_per_launch / (dom_ms * 1e-3 / len(MS)) / 1e9
+    roofline = {"kernel": "w8a8_gemm_kernel (K=1024, N=32768, M in 1..64)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": hbm_peak, "peak_source": peak_src + " hbm_gbs",
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 3),
+                "traffic": traffic_for("w8a8_gemm_kernel@K1024xN32768",
+                                       ["fp8_dynamic_quant_gb300/csrc/gemm_w8a8.cu",
+                                        "fp8_dynamic_quant_gb300/csrc/fq_common.cuh"]),
+                "algorithmic_bytes_per_launch": int(dom_bytes_per_launch),
+                "avg_launch_us": round(dom_ms * 1e3 / len(MS), 3)}
+
+    out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K_steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+           "config": {"workload": "INT8 W8A8 M-sweep: per-token quant, W8A8 GEMM and fused quant+GEMM on "
+                                  "(K=4096,N=1024) and (K=1024,N=32768), M in {1,2,3,4,7,8,9,16,32,64}",
+                      "linears": [list(l) for l in LINEARS], "M": MS,
+                      "bytes_per_step": sb,
+                      "l2": "each call reads its own weight copy; %d MB of weights per step (> 2x the %d MB L2) "
+                            "so every call streams weights from HBM; activations L2-hot" %
+                            (sum(K * N for (K, N) in LINEARS) * 20 // 2 ** 20, l2 // 2 ** 20),
+                      "timing": "op groups captured as CUDA graphs, replayed; CUDA events",
+                      "parallelism": "replicas" if world > 1 else "single GPU"},
+           "gpu_launches": launches_per_step * K_steps,
+           "groups": group_report, "roofline": roofline}
+    clk = clocks.summary(w0, w1)
+    out["clocks"] = clk
+
+    if rank == 0 and not args.no_extras:
+        out["per_call"] = per_call_breakdown(fq, torch, dev, W, SW, X, XQ, SX, Y, YF, ws, hbm_peak)
+        out["other_configs"] = other_configs(fq, synth, torch, dev, bf, l2, hbm_peak)
+        out["e2e"] = e2e(fq, torch, dev, W, SW, X, ws, args)
+    else:
+        out["e2e"] = e2e(fq, torch, dev, W, SW, X, ws, args) if rank == 0 else None
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    return out
+
+
+def time_graph(torch, fn, reps=3, calls=1):
+    """Capture fn() in a CUDA graph and return microseconds per call (median of reps replays)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3 / calls)
+    return statistics.median(ts)
+
+
+def per_call_breakdown(fq, torch, dev, W, SW, X, XQ, SX, Y, YF, ws, hbm_peak):
+    """Microseconds and GB/s per call for every (op, linear, M), each call on a different weight copy."""
+    res = {}
+    for (K, N) in LINEARS:
+        nc = len(W[(K, N)])
+        key = "K%d_N%d" % (K, N)
+        res[key] = {"M": MS, "quant_us": [], "gemm_us": [], "fused_us": [], "gemm_GBps": [], "fused_GBps": [],
+                    "gemm_frac_hbm": [], "fused_frac_hbm": [], "weight_copies_per_graph": nc}
+        for M in MS:
+            R = 16
+            tq = time_graph(torch, lambda: [fq.dynamic_quant_int8(X[(K, N, M)], XQ[(K, N, M)], SX[(K, N, M)])
+                                            for _ in range(R)], calls=R)
+            tg = time_graph(torch, lambda: [fq.w8a8_linear(XQ[(K, N, M)], SX[(K, N, M)], W[(K, N)][c], SW[(K, N)][c],
+                                                           y=Y[(K, N, M)], ws=ws) for c in range(nc)], calls=nc)
+            tf = time_graph(torch, lambda: [fq.w8a8_quant_linear(X[(K, N, M)], W[(K, N)][c], SW[(K, N)][c],
+                                                                 y=YF[(K, N, M)], ws=ws) for c in range(nc)], calls=nc)
+            gb = bytes_gemm(M, K, N) / (tg * 1e-6) / 1e9
+            fb = bytes_fused(M, K, N) / (tf * 1e-6) / 1e9
+            res[key]["quant_us"].append(round(tq, 2))
+            res[key]["gemm_us"].append(round(tg, 2))
+            res[key]["fused_us"].append(round(tf, 2))
+            res[key]["gemm_GBps"].append(round(gb, 1))
+            res[key]["fused_GBps"].append(round(fb, 1))
+            res[key]["gemm_frac_hbm"].append(round(gb / hbm_peak, 3))
+            res[key]["fused_frac_hbm"].append(round(fb / hbm_peak, 3))
+    return res
+
+
+def other_configs(fq, synth, torch, dev, bf, l2, hbm_peak):
+    import numpy as np
+    res = {}
+    # --- FP8 per-128 group quant with packed UE8M0 scales, G=8, D=4096
+    G, D = 8, 4096
+    fp8q = {}
+    for T in [1, 3, 4, 17, 128, 4096]:
+        copies = max(1, -(-2 * l2 // (2 * T * G * D)))
+        copies = min(copies, 8)
+        xs = [bf(synth.group_activations(T, G, D, SEED + 2 + c)) for c in range(copies)]
+        xq = torch.empty((T, G, D), dtype=torch.float8_e4m3fn, device=dev)
+        st = torch.empty((G, 8, (T + 3) // 4 * 4), dtype=torch.int32, device=dev)
+        R = max(copies, 8)
+        us = time_graph(torch, lambda: [fq.quant_fp8_group_ue8m0_packed(xs[i % copies], xq, st) for i in range(R)],
+                        calls=R)
+        gb = bytes_group_quant(T, G, D) / (us * 1e-6) / 1e9
+        fp8q[str(T)] = {"us": round(us, 2), "GBps": round(gb, 1), "frac_hbm": round(gb / hbm_peak, 3)}
+        del xs
+    res["fp8_group_quant_ue8m0_packed_G8_D4096"] = fp8q
+    # --- per-token INT8 quant at a size where HBM matters: M=16384, K=4096 (201 MB moved)
+    M, K = 16384, 4096
+    xs = [bf(synth.activations(M, K, SEED + 9 + c)) for c in range(2)]
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+    sx = torch.empty((M,), dtype=torch.float32, device=dev)
+    us = time_graph(torch, lambda: [fq.dynamic_quant_int8(xs[i % 2], xq, sx) for i in range(4)], calls=4)
+    gb = bytes_quant(M, K) / (us * 1e-6) / 1e9
+    res["int8_quant_M16384_K4096"] = {"us": round(us, 2), "GBps": round(gb, 1), "frac_hbm": round(gb / hbm_peak, 3)}
+    del xs
+    # --- block-scaled FP8 einsum (wo_a-like), W [8, 4096, 1024], both scale formats; and the repack control
+    N = 1024
+    ncp = max(2, -(-2 * l2 // (G * D * N)) + 1)
+    wq, sw = [], []
+    for c in range(ncp):
+        w = torch.randn((G, N, D), generator=torch.Generator(device=dev).manual_seed(SEED + 50 + c),
+                        device=dev, dtype=torch.float32) * 0.02
+        a, b = fq.quantize_weight_fp8_block(w)
+        wq.append(a)
+        sw.append(b)
+        del w
+    ein = {}
+    for T in [1, 4, 16, 64, 256]:
+        x = bf(synth.group_activations(T, G, D, SEED + 3 + T))
+        xq8, st = fq.quant_fp8_group_ue8m0_packed(x)
+        _, s32 = fq.quant_fp8_group_fp32(x)
+        y = torch.empty((T, G, N), dtype=torch.bfloat16, device=dev)
+        wsz = fq.new_workspace(fq.workspace_bytes(fq.OP_FP8_GROUP_EINSUM, T, D, N, G), dev)
+        tp = time_graph(torch, lambda: [fq.fp8_group_einsum(xq8, st, fq.SCALE_UE8M0_PACKED, wq[c], sw[c], y=y, ws=wsz)
+                                        for c in range(ncp)], calls=ncp)
+        tf = time_graph(torch, lambda: [fq.fp8_group_einsum(xq8, s32, fq.SCALE_FP32, wq[c], sw[c], y=y, ws=wsz)
+                                        for c in range(ncp)], calls=ncp)
+        # decode-step A/B: producer writes packed scales directly, vs fp32 scales + separate repack
+        xqa = torch.empty_like(xq8)
+        sta = torch.empty_like(st)
+        s32a = torch.empty_like(s32)
+        t_direct = time_graph(torch, lambda: [(fq.quant_fp8_group_ue8m0_packed(x, xqa, sta),
+                                               fq.fp8_group_einsum(xqa, sta, fq.SCALE_UE8M0_PACKED, wq[c], sw[c],
+                                                                   y=y, ws=wsz)) for c in range(ncp)], calls=ncp)
+        t_control = time_graph(torch, lambda: [(fq.quant_fp8_group_fp32(x, xqa, s32a), fq.pack_scales_ue8m0(s32a, sta),
+                                                fq.fp8_group_einsum(xqa, sta, fq.SCALE_UE8M0_PACKED, wq[c], sw[c],
+                                                                    y=y, ws=wsz)) for c in range(ncp)], calls=ncp)
+        nbytes = bytes_einsum(T, G, D, N)
+        gb = nbytes / (tp * 1e-6) / 1e9
+        flops = 2.0 * T * G * D * N
+        ein[str(T)] = {"packed_us": round(tp, 2), "fp32_us": round(tf, 2), "GBps": round(gb, 1),
+                       "frac_hbm": round(gb / hbm_peak, 3), "TFLOPs": round(flops / (tp * 1e-6) / 1e12, 1),
+                       "quant_plus_einsum_us": round(t_direct, 2),
+                       "control_quant_fp32_repack_einsum_us": round(t_control, 2)}
+    res["fp8_group_einsum_G8_D4096_N1024"] = ein
+    del wq, sw
+    # --- MoE expert chain: 256 tokens, hidden 4096, 256 experts, top-8 Zipf(1.1), intermediate 2048
+    T, topk, E, H, I = 256, 8, 256, 4096, 2048
+    c = synth.moe_case(T, topk, E, H, I, SEED + 4, with_weights=False)
+    Wd = synth.moe_weights_device(E, H, I, SEED + 4, dev)
+    x = bf(c["x"])
+    ids = torch.from_numpy(c["topk_ids"]).to(dev)
+    tw = torch.from_numpy(c["topk_w"]).to(dev)
+    bufs = fq.MoEBuffers(T, topk, E, H, I, dev)
+    us = time_graph(torch, lambda: fq.moe_forward(x, ids, tw, Wd["w13"], Wd["sw13"], Wd["w2"], Wd["sw2"], bufs=bufs),
+                    reps=5)
+    touched = int(np.unique(c["topk_ids"]).size)
+    R = T * topk
+    wbytes = touched * (2 * I * H + H * I + 4 * (2 * I + H))
+    abytes = (3 * T * H + 4 * T) + 2 * R * H + (R * H + 2 * R * 2 * I) + (2 * R * 2 * I + R * I) + \
+        (R * I + 2 * R * H) + (2 * R * H + 2 * T * H)
+    gb = (wbytes + abytes) / (us * 1e-6) / 1e9
+    res["moe_chain_T256_E256_top8"] = {"us": round(us, 1), "touched_experts": touched, "GBps": round(gb, 1),
+                                       "frac_hbm": round(gb / hbm_peak, 3),
+                                       "algorithmic_bytes": int(wbytes + abytes)}
+    del Wd, bufs
+    torch.cuda.empty_cache()
+    return res
+
+
+def e2e(fq, torch, dev, W, SW, X, ws, args):
+    """The headline step through the public API with host buffers: every call's
+    inputs are copied from pinned host memory and its results read back."""
+    import numpy as np
+    host = {}
+    for k, x in X.items():
+        K, N, M = k
+        host[k] = dict(x=x.cpu().pin_memory(), xq=torch.empty((M, K), dtype=torch.int8).pin_memory(),
+                       sx=torch.empty((M,), dtype=torch.float32).pin_memory(),
+                       y=torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
+                       yf=torch.empty((M, N), dtype=torch.bfloat16).pin_memory())
+    h2d = d2h = 0
+    for (K, N) in LINEARS:
+        for M in MS:
+            h2d += 2 * M * K + (M * K + 4 * M) + 2 * M * K
+            d2h += (M * K + 4 * M) + 2 * M * N + 2 * M * N
+
+    def one_step():
+        for (K, N) in LINEARS:
+            for i, M in enumerate(MS):
+                h = host[(K, N, M)]
+                xd = h["x"].to(dev, non_blocking=True)
+                xq, sx = fq.dynamic_quant_int8(xd)
+                h["xq"].copy_(xq, non_blocking=True)
+                h["sx"].copy_(sx, non_blocking=True)
+                xq2 = h["xq"].to(dev, non_blocking=True)
+                sx2 = h["sx"].to(dev, non_blocking=True)
+                y = fq.w8a8_linear(xq2, sx2, W[(K, N)][i], SW[(K, N)][i], ws=ws)
+                h["y"].copy_(y, non_blocking=True)
+                x3 = h["x"].to(dev, non_blocking=True)
+                yf = fq.w8a8_quant_linear(x3, W[(K, N)][10 + i], SW[(K, N)][10 + i], ws=ws)
+                h["yf"].copy_(yf, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        one_step()
+    n = max(3, min(50, args.steps // 20))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        one_step()
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(step_bytes() / dt / 1e9, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3), "steps": n,
+            "how": "eager public-API calls, pinned host buffers, H2D/D2H inside the timed loop, wall clock"}
+
+
+# ---------------------------------------------------------------- the oracle (CPU baseline / reference arm)
+def oracle_calls():
+    """The headline step as a list of oracle calls: (label, fn, algorithmic bytes)."""
+    import numpy as np
+    from fp8_dynamic_quant_gb300 import synth
+    from oracle import int8 as oi8
+    calls = []
+    for (K, N) in LINEARS:
+        w = synth.uniform_int8((N, K), SEED + K + N)
+        sw = synth.channel_scales(N, SEED + 7 + N)
+        for M in MS:
+            x = synth.activations(M, K, SEED + 1000 + M + K)
+            q, s = oi8.dynamic_quant_int8(x)
+            calls.append(("quant", (lambda x=x: oi8.dynamic_quant_int8(x)), bytes_quant(M, K)))
+            calls.append(("gemm", (lambda q=q, s=s, w=w, sw=sw: oi8.w8a8_linear(q, s, w, sw)), bytes_gemm(M, K, N)))
+            calls.append(("fused", (lambda x=x, w=w, sw=sw: oi8.w8a8_quant_linear(x, w, sw)), bytes_fused(M, K, N)))
+    return calls
+
+
+def cpu_baseline(budget_s=20.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of the headline step."""
+    calls = oracle_calls()
+    done_bytes, n, t0 = 0, 0, time.perf_counter()
+    i = 0
+    while True:
+        _, fn, b = calls[i % len(calls)]
+        fn()
+        done_bytes += b
+        n += 1
+        i += 1
+        if time.perf_counter() - t0 >= budget_s or n >= len(calls):
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d of the %d oracle calls of one headline step (quant, GEMM, fused per linear and M), "
+                      "%.1f s of CPU time, numpy with the host BLAS threads" % (n, len(calls), dt)}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, each step a bounded sample of the headline workload."""
+    calls = oracle_calls()
+    budget_total = float(os.environ.get("FQ_REF_BUDGET_S", "120"))
+    per_step = max(0.002, budget_total / max(1, args.steps + args.warmup))
+    i = 0
+
+    def one_step():
+        nonlocal i
+        t0 = time.perf_counter()
+        b = 0
+        while True:
+            _, fn, nb = calls[i % len(calls)]
+            fn()
+            b += nb
+            i += 1
+            if time.perf_counter() - t0 >= per_step:
+                return b
+
+    for _ in range(args.warmup):
+        one_step()
+    tot_b, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        tot_b += one_step()
+    dt = time.perf_counter() - t0
+    v = tot_b / dt / 1e9
+    sample = "each step runs oracle calls of the headline sweep round-robin for >= %.3f s; %d calls in all" % (per_step, i)
+    return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic", "impl": "reference",
+            "config": {"workload": "INT8 W8A8 M-sweep: per-token quant, W8A8 GEMM and fused quant+GEMM on "
+                                   "(K=4096,N=1024) and (K=1024,N=32768), M in {1,2,3,4,7,8,9,16,32,64}",
+                       "linears": [list(l) for l in LINEARS], "M": MS},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["fq", "reference"], default="fq")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-call table, other configs and e2e")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend="nccl")
+    out = run_fq(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,182 @@
+// Shared device helpers and host-side plumbing for the fq library (sm_103a).
+//
+// Everything here is infrastructure: inline-PTX wrappers for mbarriers, TMA
+// (cp.async.bulk.tensor), programmatic dependent launch, and the host
+// validation / launch helpers used by every entry point.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cstdint>
+#include <cstddef>
+
+#include "../../include/fq.h"
+
+namespace fq {
+
+// ------------------------------------------------------------ device error word
+// Bit flags OR-ed into the per-device error word.
+enum : uint32_t {
+  DEVERR_TIMEOUT = 1u,        // a bounded mbarrier wait gave up
+  DEVERR_BAD_EXPERT_ID = 2u,  // moe_sort met an id outside [0, E)
+};
+
+// Wall-clock bound of every device-side wait (nanoseconds, %globaltimer).
+constexpr uint64_t kWaitNs = 200ull * 1000ull * 1000ull;
+
+// ------------------------------------------------------------ small device helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on phase `parity`; false if it did not complete within kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitNs) return false;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------ TMA (tensor copies)
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+// 2-D tiled load global -> shared, completion counted on `bar` in bytes.
+// x is the innermost coordinate (in elements); for 8-bit data it must be a
+// multiple of 16 (every caller passes multiples of 128).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ------------------------------------------------------------ programmatic dependent launch
+// Wait until the preceding kernel in the stream has finished and its writes
+// are visible (no-op when the launch was not programmatic).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream to start launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Named barrier among `nthreads` threads (a multiple of 32), id 1..15.
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------ host side
+// Device properties of the current device, cached per device id.
+struct DevInfo {
+  int id = -1;
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  size_t smem_optin = 0;
+  uint32_t* err_word = nullptr;  // device address of this device's error word
+};
+// Fills *info for the current device; FQ_ERR_UNSUPPORTED_DEVICE unless sm_103.
+fq_status device_info(DevInfo* info);
+
+// Records a CUDA error for fq_last_cuda_error() and maps it to a status.
+fq_status cuda_status(cudaError_t e);
+
+// Encodes a 2-D 8-bit tensor map (inner dimension `cols` bytes, `rows` rows,
+// row pitch `pitch` bytes) with a box of box_cols x box_rows and 128-byte
+// swizzle; cached per thread by (ptr, sizes).  Returns nullptr on failure.
+const CUtensorMap* tensor_map_u8_2d(const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
+                                    uint32_t box_cols, uint32_t box_rows);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch with (optional) programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Whether launches may use programmatic dependent launch (env FQ_PDL=0 turns it off).
+bool pdl_enabled();
+
+}  // namespace fq
+
+namespace fq {
+// Every workspace starts with the same fixed block of per-tile arrival
+// counters (kMaxTiles words), so workspaces can be shared by different ops
+// and shapes: scratch of one call never lands on the counters of another.
+constexpr int64_t kMaxTiles = 65536;
+constexpr size_t kCounterBytes = size_t(kMaxTiles) * 4;
+// Workspace sizes of each op (bytes), for the current device.
+size_t ws_w8a8_linear(int64_t M, int64_t K, int64_t N);
+size_t ws_w8a8_quant_linear(int64_t M, int64_t K, int64_t N);
+size_t ws_fp8_group_einsum(int64_t T, int64_t D, int64_t N, int64_t G);
+size_t ws_w8a8_grouped_linear(int64_t R, int64_t K, int64_t N, int64_t E);
+constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+}  // namespace fq

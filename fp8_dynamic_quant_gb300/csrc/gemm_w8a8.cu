@@ -1,0 +1,602 @@
+// W8A8 linear for decode-sized M on sm_103a: dense (w8a8_linear), fused with
+// the per-token quant (w8a8_quant_linear) and grouped per expert
+// (w8a8_grouped_linear).
+//
+// What is computed ("DeepSeek-V4 W8A8 performance analysis", section 1):
+//   acc[m, n] = sum_k xq[m, k] * W[k, n]        exact int32
+//   y[m, n]   = bf16_RN((fp32(acc) * sx[m]) * sw[n])
+//
+// How (GB300 design, not the pages' Ascend tiling):
+//  * Swap-AB: weight rows (output channels) are the MMA "M" side, decode
+//    tokens the narrow "N" side, so a tile is 128 channels x MT tokens
+//    (MT = 8/16/32/64) and the weight stream is the only large operand.
+//  * Engine: sm_103a has no tcgen05 int8 MMA and its legacy int8 mma.sync
+//    runs at ~150 TOPS, while f16 mma.sync runs at ~600 TFLOPS.  int8 values
+//    are exact in f16 and their products and sums are exact integers in the
+//    fp32 accumulator while |partial| < 2^24, so every 8 k-blocks (1024 K,
+//    |partial| <= 1024*127*127 < 2^24) the fp32 accumulator is folded into an
+//    int32 one: the GEMM stays exact.  int8 -> f16 is a byte permute onto the
+//    f16 pattern of 1024 + (q + 128) followed by one f16x2 subtract.
+//  * Operand staging: a producer warp streams 128x128-byte weight boxes and
+//    MTx128-byte activation boxes with TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle) into a multi-stage mbarrier ring; eight consumer warps each own
+//    16 channels.  Because the K order inside a sum is free, each lane reads
+//    one contiguous 16-byte chunk per row and the same physical-to-logical K
+//    permutation is applied to both operands, so no shuffles are needed.
+//  * Scheduling: stream-K.  The (tile, k-block) iteration space is cut into
+//    equal contiguous ranges, one per CTA (one CTA per SM), which balances
+//    any (M, N, K) across all 152 SMs - the role the pages give to baseM /
+//    SmallMN / StreamK tiling ("QuantMatmul small-M tiling", section 3).
+//    A CTA's first and last tiles may be partial: their int32 partials go to
+//    per-CTA workspace slots, and the last CTA to finish a tile (counted with
+//    an atomic per tile) adds them up and runs the dequant epilogue.  Integer
+//    sums make the result independent of that order.
+//  * Weights are read with an L2 evict-first hint; activations evict-last.
+//  * Programmatic dependent launch: weight loads for the first stages are
+//    issued before griddepcontrol.wait, overlapping the previous kernel.
+#include <cuda_fp16.h>
+
+#include "fq_common.cuh"
+
+namespace fq {
+
+constexpr int kBN = 128;             // weight rows (channels) per tile
+constexpr int kBK = 128;             // K bytes per k-block
+constexpr int kCW = 8;               // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;
+constexpr int kFlushBlocks = 8;      // fold fp32 -> int32 every 8 k-blocks (1024 K)
+
+template <int MT>
+struct Cfg {
+  static constexpr int NT = MT / 8;
+  static constexpr int W_BYTES = kBN * kBK;
+  static constexpr int X_BYTES = MT * kBK;
+  static constexpr int STAGE = W_BYTES + X_BYTES;           // multiple of 1024
+  static constexpr int STAGES = MT <= 16 ? 8 : 6;
+  static constexpr int EPI = kBN * MT * 2;                  // bf16 staging
+  static constexpr int SLOT = kBN * MT;                     // int32 per slot
+  static constexpr int SMEM = STAGES * STAGE + EPI + 2 * STAGES * 8 + 64 + 1024;  // + alignment slack
+};
+
+struct Problem {
+  int M, N, K, KB;          // tokens (dense) / rows (grouped), channels, depth, k-blocks
+  int m_tiles;              // dense: tiles along M
+  int n_tiles;              // tiles along N
+  int64_t total;            // dense: total iterations (tiles * KB); grouped: computed on device
+  const float* sx;          // [M] or [R]
+  const float* sw;          // [N] or [E, N]
+  uint16_t* y;              // [M, N] or [R, N]
+  int32_t* slots;           // 2 per CTA
+  uint32_t* counters;       // per tile
+  uint32_t* err;
+  const int32_t* offsets;   // grouped: [E + 1]
+  int E;                    // grouped: experts
+};
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// int8 x4 -> two f16x2: lo = (b0, b1), hi = (b2, b3), exactly.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;                 // q + 128 as an unsigned byte
+  uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);   // f16 0x64uu = 1024 + u
+  uint32_t h = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  __half2 lh = __hsub2(*reinterpret_cast<__half2*>(&l), bias);
+  __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&h), bias);
+  lo = *reinterpret_cast<uint32_t*>(&lh);
+  hi = *reinterpret_cast<uint32_t*>(&hh);
+}
+
+__device__ __forceinline__ void mma_f16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int s) {
+  return s == 0 ? v.x : (s == 1 ? v.y : (s == 2 ? v.z : v.w));
+}
+
+// Tile -> operand coordinates.
+struct TileCoord {
+  int w_row;     // first weight row in the (possibly expert-stacked) weight tensor
+  int x_row;     // first activation row
+  int rows;      // valid activation rows in this tile (<= MT)
+  int n0;        // first output channel
+  int sw_base;   // offset of this tile's expert in sw
+};
+
+template <int MT, bool GROUPED>
+__device__ __forceinline__ TileCoord decode_tile(const Problem& p, int64_t tile, const int* tile_start) {
+  TileCoord tc;
+  if (!GROUPED) {
+    const int nt = int(tile / p.m_tiles), mt = int(tile % p.m_tiles);
+    tc.w_row = nt * kBN;
+    tc.n0 = nt * kBN;
+    tc.x_row = mt * MT;
+    tc.rows = min(MT, p.M - mt * MT);
+    tc.sw_base = 0;
+  } else {
+    // binary search the expert whose tile range holds `tile`
+    int lo = 0, hi = p.E;  // tile_start[lo] <= tile < tile_start[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int r0 = p.offsets[e], me = p.offsets[e + 1] - r0;
+    const int mtn = (me + MT - 1) / MT;
+    const int local = int(tile - tile_start[e]);
+    const int nt = local / mtn, mt = local % mtn;
+    tc.w_row = e * p.N + nt * kBN;
+    tc.n0 = nt * kBN;
+    tc.x_row = r0 + mt * MT;
+    tc.rows = min(MT, me - mt * MT);
+    tc.sw_base = e * p.N;
+  }
+  return tc;
+}
+
+__device__ __forceinline__ int64_t range_begin(int64_t b, int64_t I, int64_t G) { return b * I / G; }
+// CTA whose range holds iteration i: the largest b with floor(b*I/G) <= i.
+__device__ __forceinline__ int64_t cta_of(int64_t i, int64_t I, int64_t G) { return ((i + 1) * G - 1) / I; }
+
+// ---------------------------------------------------------------- the kernel
+template <int MT, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
+  using C = Cfg<MT>;
+  constexpr int NT = C::NT, S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + S * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE + C::EPI);
+  uint64_t* empty = full + S;
+  __shared__ int s_flag;
+  __shared__ int s_issued, s_consumed;
+  __shared__ volatile int s_abort;  // set after any timed-out wait: later waits are skipped
+  __shared__ int tile_start_s[GROUPED ? 1025 : 1];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCW);
+    }
+    fence_barrier_init();
+    s_issued = 0;
+    s_consumed = 0;
+    s_abort = 0;
+  }
+  if (warp == kCW && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  pdl_launch_dependents();
+
+  int64_t I = p.total;
+  if (GROUPED) {
+    // per-expert tile counts from the device offsets (written by moe_sort)
+    pdl_wait();
+    __shared__ int wsum[kThreads / 32];
+    const int NB = p.n_tiles;
+    const int per = (p.E + kThreads - 1) / kThreads;
+    int local = 0;
+    for (int k = 0; k < per; ++k) {
+      const int e = tid * per + k;
+      if (e < p.E) {
+        const int me = p.offsets[e + 1] - p.offsets[e];
+        local += me > 0 ? NB * ((me + MT - 1) / MT) : 0;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int k = 0; k < per; ++k) {
+      const int e = tid * per + k;
+      if (e < p.E) {
+        tile_start_s[e] = run;
+        const int me = p.offsets[e + 1] - p.offsets[e];
+        run += me > 0 ? NB * ((me + MT - 1) / MT) : 0;
+      }
+    }
+    if (tid == kThreads - 1) tile_start_s[p.E] = run;
+    __syncthreads();
+    I = int64_t(tile_start_s[p.E]) * p.KB;
+  }
+  __syncthreads();
+
+  const int64_t G = gridDim.x, b = blockIdx.x;
+  const int64_t begin = range_begin(b, I, G), end = range_begin(b + 1, I, G);
+  const int KB = p.KB;
+
+  if (warp == kCW) {
+    // ------------------------------------------------ producer warp
+    if (lane == 0 && end > begin) {
+      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      const int64_t n_it = end - begin;
+      const int npre = int(n_it < S ? n_it : S);
+      bool ok = true;
+      // weights do not depend on the previous kernel: issue them first
+      for (int r = 0; r < npre; ++r) {
+        const int64_t it = begin + r;
+        const TileCoord tc = decode_tile<MT, GROUPED>(p, it / KB, tile_start_s);
+        mbar_arrive_expect_tx(&full[r], C::STAGE);
+        tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], int(it % KB) * kBK, tc.w_row, pol_w);
+      }
+      pdl_wait();
+      for (int r = 0; r < npre; ++r) {
+        const int64_t it = begin + r;
+        const TileCoord tc = decode_tile<MT, GROUPED>(p, it / KB, tile_start_s);
+        tma_load_2d(stages + r * C::STAGE + C::W_BYTES, &tmX, &full[r], int(it % KB) * kBK, tc.x_row, pol_x);
+      }
+      int64_t issued = npre;
+      for (int64_t r = npre; r < n_it; ++r) {
+        const int s = int(r % S);
+        const uint32_t ph = uint32_t((r / S - 1) & 1);
+        if (s_abort || !mbar_wait(&empty[s], ph)) {
+          if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+          s_abort = 1;
+          ok = false;
+          break;
+        }
+        const int64_t it = begin + r;
+        const TileCoord tc = decode_tile<MT, GROUPED>(p, it / KB, tile_start_s);
+        mbar_arrive_expect_tx(&full[s], C::STAGE);
+        tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], int(it % KB) * kBK, tc.w_row, pol_w);
+        tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], int(it % KB) * kBK, tc.x_row, pol_x);
+        ++issued;
+      }
+      (void)ok;
+      s_issued = int(issued);
+    }
+  } else {
+    // ------------------------------------------------ consumer warps
+    pdl_wait();
+    const int g = lane >> 2, c = lane & 3;
+    float accf[NT][4];
+    int acci[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        accf[j][r] = 0.f;
+        acci[j][r] = 0;
+      }
+    const uint32_t sbase = smem_u32(stages);
+    const uint32_t rowW0 = uint32_t((16 * warp + g) * kBK), rowW1 = rowW0 + 8 * kBK;
+    int64_t seg_kb0 = begin % KB;
+    int nk = 0;
+    bool first_seg = true;
+    int64_t consumed = 0;
+    // After a timeout (s_abort) the loop keeps its shape - same segments, same
+    // named barriers - but skips waits and math, so every warp finishes.
+    for (int64_t it = begin; it < end; ++it) {
+      const int64_t r = it - begin;
+      const int s = int(r % S);
+      bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
+      if (!ok) {
+        if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+        s_abort = 1;
+      }
+      const uint32_t st = sbase + uint32_t(s * C::STAGE);
+#pragma unroll
+      for (int h = 0; h < 2 && ok; ++h) {
+        const uint32_t q = uint32_t(((4 * h + c) ^ g) << 4);
+        const uint4 wa = lds128(st + rowW0 + q);
+        const uint4 wb = lds128(st + rowW1 + q);
+        uint4 xv[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) xv[j] = lds128(st + C::W_BYTES + uint32_t((8 * j + g) * kBK) + q);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          i8x4_to_f16(word_of(wa, ks), a0, a2);
+          i8x4_to_f16(word_of(wb, ks), a1, a3);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            uint32_t b0, b1;
+            i8x4_to_f16(word_of(xv[j], ks), b0, b1);
+            mma_f16(accf[j], a0, a1, a2, a3, b0, b1);
+          }
+        }
+      }
+      __syncwarp();
+      if (ok) {
+        if (lane == 0) mbar_arrive(&empty[s]);
+        ++consumed;
+      }
+      const int kb = int(it % KB);
+      if (++nk == kFlushBlocks || kb == KB - 1 || it == end - 1) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            acci[j][rr] += __float2int_rn(accf[j][rr]);
+            accf[j][rr] = 0.f;
+          }
+        nk = 0;
+      }
+      if (kb == KB - 1 || it == end - 1) {
+        // ---- segment end: tile (it / KB), k-blocks [seg_kb0, kb]
+        const int64_t tile = it / KB;
+        const TileCoord tc = decode_tile<MT, GROUPED>(p, tile, tile_start_s);
+        const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
+        bool do_epi = whole;
+        if (!whole) {
+          int32_t* my = p.slots + (2 * b + (first_seg ? 0 : 1)) * int64_t(C::SLOT);
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) my[((warp * NT + j) * 4 + rr) * 32 + lane] = acci[j][rr];
+          __threadfence();
+          named_bar_sync(1, kCW * 32);
+          if (tid == 0) {
+            const uint32_t nb = uint32_t(kb - seg_kb0 + 1);
+            const uint32_t old = atomicAdd(&p.counters[tile], nb);
+            const int last = (old + nb == uint32_t(KB)) ? 1 : 0;
+            if (last) {
+              __threadfence();
+              p.counters[tile] = 0;  // every contributor has arrived; ready for the next call
+            }
+            s_flag = last;
+          }
+          named_bar_sync(1, kCW * 32);
+          do_epi = s_flag != 0;
+          if (do_epi) {
+            const int64_t c0 = cta_of(tile * KB, I, G), c1 = cta_of(tile * KB + KB - 1, I, G);
+            for (int64_t cc = c0; cc <= c1; ++cc) {
+              // CTAs with an empty range (more CTAs than iterations) wrote nothing
+              if (cc == b || range_begin(cc + 1, I, G) == range_begin(cc, I, G)) continue;
+              const int64_t first_tile = range_begin(cc, I, G) / KB;
+              const int32_t* sl = p.slots + (2 * cc + (first_tile == tile ? 0 : 1)) * int64_t(C::SLOT);
+#pragma unroll
+              for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) acci[j][rr] += __ldcg(sl + ((warp * NT + j) * 4 + rr) * 32 + lane);
+            }
+          }
+        }
+        if (do_epi) {
+          // dequant into the bf16 staging tile epi[m][n], then coalesced stores
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int nl = 16 * warp + g + ((rr & 2) ? 8 : 0);
+              const int ml = 8 * j + 2 * c + (rr & 1);
+              const int n = tc.n0 + nl;
+              float v = 0.f;
+              if (ml < tc.rows && n < p.N) {
+                const float sxv = p.sx[tc.x_row + ml];
+                const float swv = p.sw[tc.sw_base + n];
+                v = __fmul_rn(__fmul_rn(__int2float_rn(acci[j][rr]), sxv), swv);
+              }
+              epi[ml * kBN + nl] = f32_to_bf16_bits(v);
+            }
+          named_bar_sync(1, kCW * 32);
+          const int ctid = tid;  // 0..255
+          for (int idx = ctid; idx < MT * (kBN / 8); idx += kCW * 32) {
+            const int ml = idx / (kBN / 8), c8 = idx % (kBN / 8);
+            const int n = tc.n0 + c8 * 8;
+            if (ml < tc.rows && n < p.N) {
+              const uint4 v = *reinterpret_cast<const uint4*>(epi + ml * kBN + c8 * 8);
+              *reinterpret_cast<uint4*>(p.y + int64_t(tc.x_row + ml) * p.N + n) = v;
+            }
+          }
+          named_bar_sync(1, kCW * 32);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) acci[j][rr] = 0;
+        first_seg = false;
+        seg_kb0 = 0;
+      }
+    }
+    if (tid == 0) s_consumed = int(consumed);
+  }
+  __syncthreads();
+  // Drain: on the normal path every issued stage was consumed.  After a
+  // timeout, wait (bounded) for copies still in flight before exiting.
+  if (tid == 0) {
+    for (int64_t r = s_consumed; r < s_issued; ++r) mbar_wait(&full[int(r % S)], uint32_t((r / S) & 1));
+  }
+}
+
+// ---------------------------------------------------------------- host side
+static int pick_mt(int64_t M) { return M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 32 ? 32 : 64)); }
+
+static size_t slots_bytes(int sms, int mt) { return size_t(2) * sms * kBN * mt * 4; }
+
+// Workspace layout: [counters: kCounterBytes][xq, sx: fused call only][partial-sum slots]
+size_t ws_w8a8_linear(int64_t M, int64_t K, int64_t N) {
+  DevInfo d;
+  if (device_info(&d) != FQ_OK || M < 0 || K < 0 || N < 0) return 0;
+  return kCounterBytes + slots_bytes(d.sm_count, pick_mt(M));
+}
+
+size_t ws_w8a8_quant_linear(int64_t M, int64_t K, int64_t N) {
+  const size_t g = ws_w8a8_linear(M, K, N);
+  if (!g) return 0;
+  return align_up(size_t(M) * size_t(K), 256) + align_up(size_t(M) * 4, 256) + g;
+}
+
+size_t ws_w8a8_grouped_linear(int64_t R, int64_t K, int64_t N, int64_t E) {
+  DevInfo d;
+  if (device_info(&d) != FQ_OK || R < 0 || K < 0 || N < 0 || E < 0) return 0;
+  return kCounterBytes + slots_bytes(d.sm_count, 64);
+}
+
+template <int MT, bool GROUPED>
+static cudaError_t launch_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
+                               cudaStream_t s, bool pdl) {
+  auto k = w8a8_gemm_kernel<MT, GROUPED>;
+  static uint64_t attr_done = 0;  // one bit per device id
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(attr_done & (1ull << (dev & 63)))) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done |= 1ull << (dev & 63);
+  }
+  return launch(k, dim3(grid), dim3(kThreads), size_t(Cfg<MT>::SMEM), s, pdl, *tw, *tx, p);
+}
+
+// Shared by the dense and fused entry points.  `counters` is the fixed
+// counter block at the head of the workspace; `slots` the partial-sum area.
+fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K, const int8_t* w_nk, const float* sw,
+                         int64_t N, uint16_t* y, uint32_t* counters, void* slots, size_t slots_avail, cudaStream_t s,
+                         const DevInfo& d) {
+  const int mt = pick_mt(M);
+  const int64_t m_tiles = (M + mt - 1) / mt, n_tiles = (N + kBN - 1) / kBN;
+  const int64_t tiles = m_tiles * n_tiles;
+  if (tiles > kMaxTiles) return FQ_ERR_SHAPE;
+  if (slots_avail < slots_bytes(d.sm_count, mt)) return FQ_ERR_WORKSPACE;
+  Problem p = {};
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.KB = int((K + kBK - 1) / kBK);
+  p.m_tiles = int(m_tiles);
+  p.n_tiles = int(n_tiles);
+  p.total = tiles * p.KB;
+  p.sx = sx;
+  p.sw = sw;
+  p.y = y;
+  p.counters = counters;
+  p.slots = static_cast<int32_t*>(slots);
+  p.err = d.err_word;
+  const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, kBN);
+  const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
+  if (!tw || !tx) return FQ_ERR_CUDA;
+  const int grid = int(p.total < d.sm_count ? p.total : d.sm_count);
+  const bool pdl = pdl_enabled();
+  cudaError_t e;
+  switch (mt) {
+    case 8: e = launch_gemm<8, false>(tw, tx, p, grid, s, pdl); break;
+    case 16: e = launch_gemm<16, false>(tw, tx, p, grid, s, pdl); break;
+    case 32: e = launch_gemm<32, false>(tw, tx, p, grid, s, pdl); break;
+    default: e = launch_gemm<64, false>(tw, tx, p, grid, s, pdl); break;
+  }
+  return cuda_status(e);
+}
+
+}  // namespace fq
+
+using namespace fq;
+
+static fq_status check_linear_args(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K < 0 || N < 0 || K % 16 || N % 16) return FQ_ERR_SHAPE;
+  if (K > 131072 || N > (int64_t(1) << 24) || M > (int64_t(1) << 24)) return FQ_ERR_SHAPE;
+  return FQ_OK;
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status w8a8_linear(const int8_t* xq, const float* sx, int64_t M, int64_t K, const int8_t* w_nk,
+                                 const float* sw, int64_t N, uint16_t* y, void* ws, size_t ws_bytes,
+                                 fq_stream_t stream) {
+  fq_status st = check_linear_args(M, K, N);
+  if (st != FQ_OK) return st;
+  if (M == 0 || N == 0) return FQ_OK;
+  if (!xq || !sx || !w_nk || !sw || !y) return FQ_ERR_NULL;
+  if (!aligned16(xq) || !aligned16(sx) || !aligned16(w_nk) || !aligned16(sw) || !aligned16(y)) return FQ_ERR_ALIGN;
+  DevInfo d;
+  if ((st = device_info(&d)) != FQ_OK) return st;
+  if (K == 0) {
+    cudaError_t e = cudaMemsetAsync(y, 0, size_t(M) * size_t(N) * 2, reinterpret_cast<cudaStream_t>(stream));
+    return cuda_status(e);
+  }
+  if (!ws || ws_bytes < kCounterBytes) return FQ_ERR_WORKSPACE;
+  if (!aligned16(ws)) return FQ_ERR_ALIGN;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  return run_w8a8_dense(xq, sx, M, K, w_nk, sw, N, y, reinterpret_cast<uint32_t*>(w8), w8 + kCounterBytes,
+                        ws_bytes - kCounterBytes, reinterpret_cast<cudaStream_t>(stream), d);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(const uint16_t* x, int64_t M, int64_t K, const int8_t* w_nk, const float* sw,
+                                       int64_t N, uint16_t* y, int8_t* xq_out, float* sx_out, void* ws,
+                                       size_t ws_bytes, fq_stream_t stream) {
+  fq_status st = check_linear_args(M, K, N);
+  if (st != FQ_OK) return st;
+  if (M == 0) return FQ_OK;
+  if (!x || !w_nk || !sw || !y) return FQ_ERR_NULL;
+  if (!aligned16(x) || !aligned16(w_nk) || !aligned16(sw) || !aligned16(y) || (xq_out && !aligned16(xq_out)) ||
+      (sx_out && !aligned16(sx_out)))
+    return FQ_ERR_ALIGN;
+  DevInfo d;
+  if ((st = device_info(&d)) != FQ_OK) return st;
+  const size_t xq_b = align_up(size_t(M) * size_t(K), 256), sx_b = align_up(size_t(M) * 4, 256);
+  if (!ws || ws_bytes < kCounterBytes + xq_b + sx_b) return FQ_ERR_WORKSPACE;
+  if (!aligned16(ws)) return FQ_ERR_ALIGN;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  int8_t* xq = xq_out ? xq_out : reinterpret_cast<int8_t*>(w8 + kCounterBytes);
+  float* sx = sx_out ? sx_out : reinterpret_cast<float*>(w8 + kCounterBytes + xq_b);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // validate the GEMM part before launching the quant
+  if (N > 0 && K > 0 && ws_bytes - kCounterBytes - xq_b - sx_b < slots_bytes(d.sm_count, pick_mt(M)))
+    return FQ_ERR_WORKSPACE;
+  if ((st = dynamic_quant_int8(x, M, K, xq, sx, stream)) != FQ_OK) return st;
+  if (N == 0) return FQ_OK;
+  if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(M) * size_t(N) * 2, s));
+  return run_w8a8_dense(xq, sx, M, K, w_nk, sw, N, y, reinterpret_cast<uint32_t*>(w8),
+                        w8 + kCounterBytes + xq_b + sx_b, ws_bytes - kCounterBytes - xq_b - sx_b, s, d);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(const int8_t* xq, const float* sx, const int32_t* offsets, int64_t R,
+                                         int64_t E, int64_t K, const int8_t* w_enk, const float* sw_en, int64_t N,
+                                         uint16_t* y, void* ws, size_t ws_bytes, fq_stream_t stream) {
+  fq_status st = check_linear_args(R, K, N);
+  if (st != FQ_OK) return st;
+  if (E <= 0 || E > 1024 || E * N > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
+  if (R == 0 || N == 0) return FQ_OK;
+  if (K == 0) return FQ_ERR_SHAPE;
+  if (!xq || !sx || !offsets || !w_enk || !sw_en || !y) return FQ_ERR_NULL;
+  if (!aligned16(xq) || !aligned16(sx) || !aligned16(offsets) || !aligned16(w_enk) || !aligned16(sw_en) ||
+      !aligned16(y))
+    return FQ_ERR_ALIGN;
+  DevInfo d;
+  if ((st = device_info(&d)) != FQ_OK) return st;
+  constexpr int mt = 64;
+  const int64_t n_tiles = (N + kBN - 1) / kBN;
+  const int64_t max_tiles = n_tiles * ((R + mt - 1) / mt + E);
+  if (max_tiles > kMaxTiles) return FQ_ERR_SHAPE;
+  const size_t need = kCounterBytes + slots_bytes(d.sm_count, mt);
+  if (!ws || ws_bytes < need) return FQ_ERR_WORKSPACE;
+  if (!aligned16(ws)) return FQ_ERR_ALIGN;
+  Problem p = {};
+  p.M = int(R);
+  p.N = int(N);
+  p.K = int(K);
+  p.KB = int((K + kBK - 1) / kBK);
+  p.n_tiles = int(n_tiles);
+  p.m_tiles = 0;
+  p.total = 0;
+  p.sx = sx;
+  p.sw = sw_en;
+  p.y = y;
+  p.counters = static_cast<uint32_t*>(ws);
+  p.slots = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kCounterBytes);
+  p.err = d.err_word;
+  p.offsets = offsets;
+  p.E = int(E);
+  const CUtensorMap* tw = tensor_map_u8_2d(w_enk, uint64_t(K), uint64_t(E * N), uint64_t(K), kBK, kBN);
+  const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, uint32_t(mt));
+  if (!tw || !tx) return FQ_ERR_CUDA;
+  return cuda_status(
+      launch_gemm<mt, true>(tw, tx, p, d.sm_count, reinterpret_cast<cudaStream_t>(stream), pdl_enabled()));
+}

@@ -1,0 +1,552 @@
+// Quantization kernels of the decode path (sm_103a).
+//
+//  * dynamic_quant_int8      per-token INT8 quant  ("DeepSeek-V4 W8A8
+//                            performance analysis", sections 1-2)
+//  * swiglu_quant_int8       SwiGLU + per-token INT8 re-quant ("Reshaping LLM
+//                            inference dataflow: DeepSeek V4 950", section 2.3)
+//  * moe_gather_rows_i8      expert-order gather of quantized rows (same page,
+//                            section 3.2)
+//  * quant_fp8_group_*       FP8 E4M3 per-128 group quant writing packed UE8M0
+//                            scales ("SGLang PR #34277 digest", implementation
+//                            breakdown items 1-2, key source snippets)
+//  * fq_pack_scales_ue8m0    the separate fp32 -> packed conversion that the PR
+//                            removed (motivation section), kept as the A/B control
+//  * fq_quantize_weight_fp8_block   load-time fp8 weight prep
+//
+// All are HBM-streaming kernels: 16-byte coalesced loads and stores,
+// warp-shuffle reductions, grids sized to a multiple of the SM count.
+#include "fq_common.cuh"
+
+namespace fq {
+
+// ---------------------------------------------------------------- shared math
+
+// q = clamp(rint(x / s), -127, 127) with x / s the IEEE fp32 quotient, ties
+// to even.  The quotient is first estimated as x * RN(1/s) (within 2.3e-5 of
+// the IEEE quotient for |x / s| <= 127); only when that estimate lies within
+// 2^-14 of a half-integer, where the two could round differently, is the
+// exact __fdiv_rn taken.  s == 0 only for an all-zero row (q = 0).  When
+// RN(1/s) is not finite (s below ~2.9e-39) every element takes the exact path.
+__device__ __forceinline__ int quant_i8(float x, float s, float inv_s) {
+  if (s == 0.0f) return 0;
+  const float y = __fmul_rn(x, inv_s);
+  float r = rintf(y);
+  const float d = fabsf(y - r);
+  if (!(fabsf(d - 0.5f) >= (1.0f / 16384.0f))) r = rintf(__fdiv_rn(x, s));  // also catches NaN from inf
+  r = fminf(fmaxf(r, -127.0f), 127.0f);
+  return static_cast<int>(r);
+}
+
+__device__ __forceinline__ uint32_t pack4_i8(int a, int b, int c, int d) {
+  return (uint32_t(a) & 0xFFu) | ((uint32_t(b) & 0xFFu) << 8) | ((uint32_t(c) & 0xFFu) << 16) |
+         ((uint32_t(d) & 0xFFu) << 24);
+}
+
+// 8 bf16 values in a uint4 -> floats.
+__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float absmax8(const float f[8]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+  return m;
+}
+
+__device__ __forceinline__ uint2 quant8_i8(const float f[8], float s, float inv) {
+  uint2 o;
+  o.x = pack4_i8(quant_i8(f[0], s, inv), quant_i8(f[1], s, inv), quant_i8(f[2], s, inv), quant_i8(f[3], s, inv));
+  o.y = pack4_i8(quant_i8(f[4], s, inv), quant_i8(f[5], s, inv), quant_i8(f[6], s, inv), quant_i8(f[7], s, inv));
+  return o;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Block-wide max over blockDim.x threads (multiple of 32); `red` holds 32 floats.
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  float r = (lane < nw) ? red[lane] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
+  __syncthreads();  // `red` is reused by the next row
+  return r;
+}
+
+// ---------------------------------------------------------------- a1: per-token INT8
+
+// One CTA per row (grid-stride over rows).  Each thread keeps up to VPT
+// 16-byte vectors (8 bf16) of the row in registers between the absmax pass
+// and the quant pass; longer rows re-read the remainder (L2-resident).
+template <int VPT>
+__global__ void __launch_bounds__(256) dynamic_quant_int8_kernel(const uint4* __restrict__ x, int64_t M,
+                                                                  int64_t K8, uint2* __restrict__ q,
+                                                                  float* __restrict__ s) {
+  __shared__ float red[32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
+    const uint4* xr = x + row * K8;
+    uint4 v[VPT];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * nt;
+      if (idx < K8) {
+        v[i] = ld_stream(xr + idx);
+        float f[8];
+        unpack8(v[i], f);
+        amax = fmaxf(amax, absmax8(f));
+      }
+    }
+    for (int64_t idx = tid + int64_t(VPT) * nt; idx < K8; idx += nt) {
+      float f[8];
+      unpack8(xr[idx], f);
+      amax = fmaxf(amax, absmax8(f));
+    }
+    amax = block_max(amax, red);
+    const float sc = __fdiv_rn(amax, 127.0f);
+    const float inv = __frcp_rn(sc);
+    if (tid == 0) s[row] = sc;
+    uint2* qr = q + row * K8;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * nt;
+      if (idx < K8) {
+        float f[8];
+        unpack8(v[i], f);
+        qr[idx] = quant8_i8(f, sc, inv);
+      }
+    }
+    for (int64_t idx = tid + int64_t(VPT) * nt; idx < K8; idx += nt) {
+      float f[8];
+      unpack8(xr[idx], f);
+      qr[idx] = quant8_i8(f, sc, inv);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- a7: SwiGLU + INT8
+
+// h = bf16_RN(fp32(silu(g)) * u), silu(g) = g / (1 + exp(-g)); then the
+// per-token quant of h.  One CTA per row; VPT vectors of 8 outputs cached.
+__device__ __forceinline__ void swiglu8(const uint4& gv, const uint4& uv, float h[8], uint4* hbits) {
+  float g[8], u[8];
+  unpack8(gv, g);
+  unpack8(uv, u);
+  uint32_t hb[4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    // silu(g) = g / (1 + e^-g); for g < 0 the same value as g e^g / (1 + e^g),
+    // which does not overflow for large |g|
+    float sg;
+    if (g[i] >= 0.0f) {
+      sg = __fdiv_rn(g[i], __fadd_rn(1.0f, expf(-g[i])));
+    } else {
+      const float e = expf(g[i]);
+      sg = __fdiv_rn(__fmul_rn(g[i], e), __fadd_rn(1.0f, e));
+    }
+    const uint16_t b = f32_to_bf16_bits(__fmul_rn(sg, u[i]));
+    h[i] = __uint_as_float(uint32_t(b) << 16);
+    if (i & 1)
+      hb[i >> 1] |= uint32_t(b) << 16;
+    else
+      hb[i >> 1] = b;
+  }
+  *hbits = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(256) swiglu_quant_int8_kernel(const uint4* __restrict__ gu, int64_t rows,
+                                                                 int64_t I8, uint2* __restrict__ hq,
+                                                                 float* __restrict__ sh, uint4* __restrict__ hout) {
+  __shared__ float red[32];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    const uint4* gr = gu + row * 2 * I8;
+    const uint4* ur = gr + I8;
+    float h[VPT][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * nt;
+      if (idx < I8) {
+        uint4 hb;
+        swiglu8(ld_stream(gr + idx), ld_stream(ur + idx), h[i], &hb);
+        if (hout) hout[row * I8 + idx] = hb;
+        amax = fmaxf(amax, absmax8(h[i]));
+      }
+    }
+    for (int64_t idx = tid + int64_t(VPT) * nt; idx < I8; idx += nt) {
+      float t[8];
+      uint4 hb;
+      swiglu8(gr[idx], ur[idx], t, &hb);
+      if (hout) hout[row * I8 + idx] = hb;
+      amax = fmaxf(amax, absmax8(t));
+    }
+    amax = block_max(amax, red);
+    const float sc = __fdiv_rn(amax, 127.0f);
+    const float inv = __frcp_rn(sc);
+    if (tid == 0) sh[row] = sc;
+    uint2* qr = hq + row * I8;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * nt;
+      if (idx < I8) qr[idx] = quant8_i8(h[i], sc, inv);
+    }
+    for (int64_t idx = tid + int64_t(VPT) * nt; idx < I8; idx += nt) {
+      float t[8];
+      uint4 hb;
+      swiglu8(gr[idx], ur[idx], t, &hb);
+      qr[idx] = quant8_i8(t, sc, inv);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- a5: gather
+
+// Row i of the expert-ordered copy is source token perm[i] / topk.
+__global__ void __launch_bounds__(256) gather_rows_i8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx,
+                                                              const int32_t* __restrict__ perm, int64_t R,
+                                                              int64_t topk, int64_t K16, int64_t T,
+                                                              uint4* __restrict__ xg, float* __restrict__ sg) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t row = int64_t(blockIdx.x) * warps + warp; row < R; row += int64_t(gridDim.x) * warps) {
+    int64_t src = perm[row] / topk;
+    if (src < 0 || src >= T) src = 0;  // perm comes from moe_sort; stay in bounds regardless
+    if (lane == 0) sg[row] = sx[src];
+    for (int64_t c = lane; c < K16; c += 32) xg[row * K16 + c] = xq[src * K16 + c];
+  }
+}
+
+// ---------------------------------------------------------------- a3: FP8 group quant
+
+// e = clamp(ceil(log2(amax / 448)), -127, 127) from the bits of amax:
+// with amax = 1.f * 2^E, amax <= 448 * 2^k  <=>  1.f <= 1.75 * 2^(k + 8 - E),
+// so k = E - 8 when the fraction 1.f <= 1.75 (mantissa bits <= 0x600000) and
+// E - 7 otherwise.  Zero and subnormal amax fall below the clamp (-127).
+__device__ __forceinline__ int ue8m0_exp(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int E = int((b >> 23) & 0xFFu);
+  if (E == 0) return -127;
+  const int e = (E - 127) - 8 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+  return max(-127, min(127, e));
+}
+
+// 2^e as fp32 for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float exp2_int(int e) {
+  const int be = e + 127;
+  return be >= 1 ? __uint_as_float(uint32_t(be) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+// One warp per (t, g, pack p) unit: lanes 8i..8i+7 cover hidden group
+// j = 4p + i (16 elements each, two 16-byte loads), an 8-lane shuffle gives
+// the group absmax, and lane 0 assembles the four exponent bytes into one
+// int32 word.  Groups past NG contribute byte 0 (zeroed tail of the last
+// pack); token-padding units t >= T write a zero word and touch no payload.
+// PACKED = false writes fp32 scales [T, G, NG] instead (the A/B control).
+template <bool PACKED>
+__global__ void __launch_bounds__(256) quant_fp8_group_kernel(const uint4* __restrict__ x, int T, int G, int NG,
+                                                               int P, int Ta, uint4* __restrict__ xq,
+                                                               int32_t* __restrict__ s_packed,
+                                                               float* __restrict__ s_f32) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane >> 3, l8 = lane & 7;
+  const int64_t D16 = int64_t(NG) * 16;  // 16-byte vectors of bf16 per (t, g) row (8 elem each)
+  const int64_t units = PACKED ? int64_t(G) * P * Ta : int64_t(G) * P * T;
+  for (int64_t u = int64_t(blockIdx.x) * warps + warp; u < units; u += int64_t(gridDim.x) * warps) {
+    // unit order follows the scale words: ((g * P + p) * Ta + t)
+    const int tdim = PACKED ? Ta : T;
+    const int t = int(u % tdim);
+    const int64_t gp = u / tdim;
+    const int p = int(gp % P), g = int(gp / P);
+    const int j = 4 * p + sub;
+    // every lane joins the shuffles; lanes past the last group or in token
+    // padding carry zeros and store nothing
+    const bool active = (t < T) && (j < NG);
+    const int64_t vbase = (int64_t(t) * G + g) * D16 + int64_t(j) * 16 + l8 * 2;
+    float f[16];
+    if (active) {
+      const uint4 v0 = ld_stream(x + vbase), v1 = ld_stream(x + vbase + 1);
+      unpack8(v0, f);
+      unpack8(v1, f + 8);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) f[i] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int e = ue8m0_exp(amax);
+    uint32_t byte = 0;
+    if (active) {
+      const float sc = exp2_int(-e);
+      uint4 o;
+      o.x = e4m3x4(f[0] * sc, f[1] * sc, f[2] * sc, f[3] * sc);
+      o.y = e4m3x4(f[4] * sc, f[5] * sc, f[6] * sc, f[7] * sc);
+      o.z = e4m3x4(f[8] * sc, f[9] * sc, f[10] * sc, f[11] * sc);
+      o.w = e4m3x4(f[12] * sc, f[13] * sc, f[14] * sc, f[15] * sc);
+      xq[vbase / 2] = o;  // 16 E4M3 codes = one uint4 per lane
+      byte = uint32_t(e + 127);
+      if (!PACKED && l8 == 0) s_f32[(int64_t(t) * G + g) * NG + j] = exp2_int(e);
+    }
+    if (PACKED) {
+      const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, byte, 8);
+      const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, byte, 16);
+      const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, byte, 24);
+      if (lane == 0) s_packed[u] = int32_t(byte | (b1 << 8) | (b2 << 16) | (b3 << 24));
+    }
+  }
+}
+
+// fp32 power-of-two scales [T, G, NG] -> packed int32 [G, P, Ta]; one thread per word.
+__global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restrict__ s, int T, int G, int NG, int P,
+                                                           int Ta, int32_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t words = int64_t(G) * P * Ta;
+  for (int64_t w = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; w < words; w += int64_t(gridDim.x) * blockDim.x) {
+    const int t = int(w % Ta);
+    const int64_t gp = w / Ta;
+    const int p = int(gp % P), g = int(gp / P);
+    uint32_t word = 0;
+    if (t < T) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int j = 4 * p + b;
+        if (j < NG) {
+          const uint32_t bits = __float_as_uint(s[(int64_t(t) * G + g) * NG + j]) & 0x7FFFFFFFu;
+          const int E = int(bits >> 23);
+          // a power of two: normal -> E - 127; subnormal 2^k -> k = log2(mantissa) - 149
+          const int e = E ? (E - 127) : ((31 - __clz(bits)) - 149);
+          word |= uint32_t(max(-127, min(127, e)) + 127) << (8 * b);
+        }
+      }
+    }
+    out[w] = int32_t(word);
+  }
+}
+
+// ---------------------------------------------------------------- fp8 weight prep
+
+// One CTA per 128 x 128 block (rows n, columns d of w[G, N, D]).
+__global__ void __launch_bounds__(256) quantize_weight_fp8_kernel(const float4* __restrict__ w, int G, int N, int D,
+                                                                   uint32_t* __restrict__ wq, float* __restrict__ sw) {
+  __shared__ float red[32];
+  const int NB = N / 128, KB = D / 128;
+  const int b = blockIdx.x;
+  const int kb = b % KB, nb = (b / KB) % NB, g = b / (KB * NB);
+  const int tid = threadIdx.x;
+  const int64_t D4 = D / 4;
+  float4 v[16];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int f4 = tid + i * 256;           // 0..4095 float4 of the block
+    const int r = f4 >> 5, c4 = f4 & 31;    // 32 float4 per 128-wide row
+    v[i] = w[(int64_t(g) * N + nb * 128 + r) * D4 + kb * 32 + c4];
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  }
+  amax = block_max(amax, red);
+  const float s = __fdiv_rn(amax, 448.0f);
+  if (tid == 0) sw[(int64_t(g) * KB + kb) * NB + nb] = s;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int f4 = tid + i * 256;
+    const int r = f4 >> 5, c4 = f4 & 31;
+    float a = 0.f, bb = 0.f, c = 0.f, d = 0.f;
+    if (s != 0.0f) {
+      a = __fdiv_rn(v[i].x, s);
+      bb = __fdiv_rn(v[i].y, s);
+      c = __fdiv_rn(v[i].z, s);
+      d = __fdiv_rn(v[i].w, s);
+    }
+    wq[(int64_t(g) * N + nb * 128 + r) * D4 + kb * 32 + c4] = e4m3x4(a, bb, c, d);
+  }
+}
+
+static int grid_for(int64_t work, int per_cta, int sms, int ctas_per_sm) {
+  int64_t need = (work + per_cta - 1) / per_cta;
+  int64_t cap = int64_t(sms) * ctas_per_sm;
+  return int(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+}  // namespace fq
+
+using namespace fq;
+
+// ================================================================ entry points
+
+extern "C" __attribute__((visibility("default"))) fq_status dynamic_quant_int8(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx,
+                                        fq_stream_t stream) {
+  if (M < 0 || K < 0 || K % 16 || K > (int64_t(1) << 30) || M > (int64_t(1) << 40)) return FQ_ERR_SHAPE;
+  if (M == 0) return FQ_OK;
+  if (!x || !xq || !sx) return FQ_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xq) || !aligned16(sx)) return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t K8 = K / 8;
+  const int threads = K8 >= 256 ? 256 : (K8 >= 128 ? 128 : (K8 >= 64 ? 64 : 32));
+  const int grid = grid_for(M, 1, d.sm_count, 2048 / threads);
+  const int64_t vpt = (K8 + threads - 1) / threads;
+  const bool pdl = pdl_enabled();
+  cudaError_t e;
+  auto xp = reinterpret_cast<const uint4*>(x);
+  auto qp = reinterpret_cast<uint2*>(xq);
+  if (vpt <= 1)
+    e = launch(dynamic_quant_int8_kernel<1>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+  else if (vpt <= 2)
+    e = launch(dynamic_quant_int8_kernel<2>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+  else if (vpt <= 4)
+    e = launch(dynamic_quant_int8_kernel<4>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+  else
+    e = launch(dynamic_quant_int8_kernel<8>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+  return cuda_status(e);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status swiglu_quant_int8(const uint16_t* gu, int64_t rows, int64_t I, int8_t* hq, float* sh,
+                                       uint16_t* h_out, fq_stream_t stream) {
+  if (rows < 0 || I < 0 || I % 16 || I > (int64_t(1) << 28)) return FQ_ERR_SHAPE;
+  if (rows == 0 || I == 0) return FQ_OK;
+  if (!gu || !hq || !sh) return FQ_ERR_NULL;
+  if (!aligned16(gu) || !aligned16(hq) || !aligned16(sh) || (h_out && !aligned16(h_out))) return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t I8 = I / 8;
+  const int threads = I8 >= 256 ? 256 : (I8 >= 128 ? 128 : (I8 >= 64 ? 64 : 32));
+  const int grid = grid_for(rows, 1, d.sm_count, 2048 / threads);
+  const int64_t vpt = (I8 + threads - 1) / threads;
+  const bool pdl = pdl_enabled();
+  auto gp = reinterpret_cast<const uint4*>(gu);
+  auto qp = reinterpret_cast<uint2*>(hq);
+  auto hp = reinterpret_cast<uint4*>(h_out);
+  cudaError_t e;
+  if (vpt <= 1)
+    e = launch(swiglu_quant_int8_kernel<1>, grid, threads, 0, s, pdl, gp, rows, I8, qp, sh, hp);
+  else if (vpt <= 2)
+    e = launch(swiglu_quant_int8_kernel<2>, grid, threads, 0, s, pdl, gp, rows, I8, qp, sh, hp);
+  else
+    e = launch(swiglu_quant_int8_kernel<4>, grid, threads, 0, s, pdl, gp, rows, I8, qp, sh, hp);
+  return cuda_status(e);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status moe_gather_rows_i8(const int8_t* xq, const float* sx, const int32_t* perm, int64_t T,
+                                        int64_t topk, int64_t K, int8_t* xq_g, float* sx_g, fq_stream_t stream) {
+  if (T < 0 || topk <= 0 || K < 0 || K % 16 || T * topk > (int64_t(1) << 31)) return FQ_ERR_SHAPE;
+  const int64_t R = T * topk;
+  if (R == 0) return FQ_OK;
+  if (!xq || !sx || !perm || !xq_g || !sx_g) return FQ_ERR_NULL;
+  if (!aligned16(xq) || !aligned16(xq_g) || !aligned16(perm) || !aligned16(sx) || !aligned16(sx_g))
+    return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  const int grid = grid_for(R, 8, d.sm_count, 8);
+  return cuda_status(launch(gather_rows_i8_kernel, grid, 256, 0, reinterpret_cast<cudaStream_t>(stream),
+                            pdl_enabled(), reinterpret_cast<const uint4*>(xq), sx, perm, R, topk, K / 16, T,
+                            reinterpret_cast<uint4*>(xq_g), sx_g));
+}
+
+static fq_status fp8_group_common(const uint16_t* x, int64_t T, int64_t G, int64_t D, uint8_t* xq, int32_t* sp,
+                                  float* sf, fq_stream_t stream, bool packed) {
+  if (T < 0 || G < 0 || D < 0 || D % 128 || T > (int64_t(1) << 30) || G > (int64_t(1) << 20) ||
+      D > (int64_t(1) << 24))
+    return FQ_ERR_SHAPE;
+  const int64_t NG = D / 128, P = (NG + 3) / 4, Ta = (T + 3) / 4 * 4;
+  if (G == 0 || D == 0 || T == 0) return FQ_OK;  // T == 0: the [G, P, 0] storage is empty
+  if (!x || !xq || (packed ? !sp : !sf)) return FQ_ERR_NULL;
+  if (!aligned16(x) || !aligned16(xq) || (sp && !aligned16(sp)) || (sf && !aligned16(sf))) return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t units = G * P * (sp ? Ta : T);
+  if (units == 0) return FQ_OK;
+  const int grid = grid_for(units, 8, d.sm_count, 8);
+  cudaError_t e;
+  if (sp)
+    e = launch(quant_fp8_group_kernel<true>, grid, 256, 0, s, pdl_enabled(), reinterpret_cast<const uint4*>(x),
+               int(T), int(G), int(NG), int(P), int(Ta), reinterpret_cast<uint4*>(xq), sp, (float*)nullptr);
+  else
+    e = launch(quant_fp8_group_kernel<false>, grid, 256, 0, s, pdl_enabled(), reinterpret_cast<const uint4*>(x),
+               int(T), int(G), int(NG), int(P), int(Ta), reinterpret_cast<uint4*>(xq), (int32_t*)nullptr, sf);
+  return cuda_status(e);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status quant_fp8_group_ue8m0_packed(const uint16_t* x, int64_t T, int64_t G, int64_t D,
+                                                  uint8_t* xq, int32_t* s_packed, fq_stream_t stream) {
+  return fp8_group_common(x, T, G, D, xq, s_packed, nullptr, stream, true);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status quant_fp8_group_fp32(const uint16_t* x, int64_t T, int64_t G, int64_t D, uint8_t* xq,
+                                          float* s_f32, fq_stream_t stream) {
+  return fp8_group_common(x, T, G, D, xq, nullptr, s_f32, stream, false);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status fq_pack_scales_ue8m0(const float* s_f32, int64_t T, int64_t G, int64_t NG, int32_t* s_packed,
+                                          fq_stream_t stream) {
+  if (T < 0 || G < 0 || NG < 0 || T > (int64_t(1) << 30) || G > (int64_t(1) << 20) || NG > (int64_t(1) << 20))
+    return FQ_ERR_SHAPE;
+  const int64_t P = (NG + 3) / 4, Ta = (T + 3) / 4 * 4;
+  const int64_t words = G * P * Ta;
+  if (words == 0) return FQ_OK;
+  if (!s_packed || (!s_f32 && T > 0)) return FQ_ERR_NULL;
+  if (!aligned16(s_packed) || (s_f32 && !aligned16(s_f32))) return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  const int grid = grid_for(words, 256, d.sm_count, 8);
+  return cuda_status(launch(pack_scales_kernel, grid, 256, 0, reinterpret_cast<cudaStream_t>(stream), pdl_enabled(),
+                            s_f32, int(T), int(G), int(NG), int(P), int(Ta), s_packed));
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status fq_quantize_weight_fp8_block(const float* w_gnd, int64_t G, int64_t N, int64_t D, uint8_t* wq,
+                                                  float* sw_blk, fq_stream_t stream) {
+  if (G < 0 || N < 0 || D < 0 || N % 128 || D % 128 || G * (N / 128) * (D / 128) > (int64_t(1) << 31))
+    return FQ_ERR_SHAPE;
+  const int64_t blocks = G * (N / 128) * (D / 128);
+  if (blocks == 0) return FQ_OK;
+  if (!w_gnd || !wq || !sw_blk) return FQ_ERR_NULL;
+  if (!aligned16(w_gnd) || !aligned16(wq) || !aligned16(sw_blk)) return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  return cuda_status(launch(quantize_weight_fp8_kernel, int(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream),
+                            false, reinterpret_cast<const float4*>(w_gnd), int(G), int(N), int(D),
+                            reinterpret_cast<uint32_t*>(wq), sw_blk));
+}

@@ -40,8 +40,30 @@ def activations(M, K, seed, outlier_p=0.001, outlier_mul=50.0):
     return to_bf16_bits(x)
 
 
+def uniform_int8(shape, seed):
+    """int8 uniform on [-127, 127] (host)."""
+    return rng(seed).integers(-127, 128, size=shape, dtype=np.int8)
+
+
+def uniform_int8_device(shape, seed, device):
+    """int8 uniform on [-127, 127], drawn by torch's seeded generator on `device`.
+
+    Used for multi-GB expert weights; tests hand host copies of the slices
+    they check to the oracle.
+    """
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randint(-127, 128, tuple(shape), generator=g, dtype=torch.int8, device=device)
+
+
+def uniform_f32_device(shape, lo, hi, seed, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.rand(tuple(shape), generator=g, dtype=torch.float32, device=device) * (hi - lo) + lo
+
+
 def int8_weights(N, K, seed):
-    return rng(seed).integers(-127, 128, size=(N, K), dtype=np.int8)
+    return uniform_int8((N, K), seed)
 
 
 def channel_scales(N, seed, lo=1e-3, hi=1e-2):
@@ -91,12 +113,20 @@ def topk_weights(T, topk, seed):
 
 
 def moe_case(T, topk, E, H, I, seed, with_weights=True):
-    """Decode MoE batch: tokens, routing, and expert weights."""
+    """Decode MoE batch: tokens, routing, and (host) expert weights."""
     c = dict(x=activations(T, H, seed), topk_ids=zipf_topk(T, topk, E, seed + 1),
              topk_w=topk_weights(T, topk, seed + 2))
     if with_weights:
-        c.update(w13=rng(seed + 3).integers(-127, 128, size=(E, 2 * I, H), dtype=np.int8),
+        c.update(w13=uniform_int8((E, 2 * I, H), seed + 3),
                  sw13=rng(seed + 4).uniform(1e-3, 1e-2, size=(E, 2 * I)).astype(np.float32),
-                 w2=rng(seed + 5).integers(-127, 128, size=(E, H, I), dtype=np.int8),
+                 w2=uniform_int8((E, H, I), seed + 5),
                  sw2=rng(seed + 6).uniform(1e-3, 1e-2, size=(E, H)).astype(np.float32))
     return c
+
+
+def moe_weights_device(E, H, I, seed, device):
+    """Expert weights on the device: W13 int8 [E, 2I, H], sw13 [E, 2I], W2 int8 [E, H, I], sw2 [E, H]."""
+    return dict(w13=uniform_int8_device((E, 2 * I, H), seed + 3, device),
+                sw13=uniform_f32_device((E, 2 * I), 1e-3, 1e-2, seed + 4, device),
+                w2=uniform_int8_device((E, H, I), seed + 5, device),
+                sw2=uniform_f32_device((E, H), 1e-3, 1e-2, seed + 6, device))

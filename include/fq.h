@@ -1,0 +1,258 @@
+/*
+ * fq.h - C ABI of the GB300 (sm_103a) decode quant + quantized-linear library.
+ *
+ * One process, one GPU.  Every entry point is asynchronous on the caller's
+ * CUDA stream, takes plain pointers and sizes, allocates nothing, and
+ * returns an fq_status.  No exception crosses this boundary and nothing
+ * aborts.
+ *
+ * Sources (page title, then section), cited per entry point below:
+ *   [W8A8] "DeepSeek-V4 W8A8 performance analysis: small M, NZ layout and
+ *          measurement method".
+ *   [PR]   "SGLang PR #34277 digest: the DSV4 FP8 quant kernel writes
+ *          DeepGEMM's TMA-aligned packed UE8M0 scales".
+ *   [DF]   "Reshaping LLM inference dataflow: DeepSeek V4 950 low-precision
+ *          optimisation retrospective".
+ *
+ * Conventions shared by all entry points
+ *   - Pointers named x, xq, w, y, s, ... are DEVICE pointers owned by the
+ *     caller, valid for the sizes stated, and 16-byte aligned (the
+ *     analogue of the 16-byte output_s check in [PR] implementation
+ *     breakdown item 1).  A misaligned pointer returns FQ_ERR_ALIGN.
+ *   - bf16 values travel as uint16_t bit patterns, E4M3 values as uint8_t
+ *     codes, UE8M0 scales as bytes packed four to an int32.
+ *   - Row-major ("C") layouts.  Weights are stored K-major: the logical
+ *     W[k, n] of a linear is w_nk[n * K + k].  This is the one-time,
+ *     load-time layout choice that plays the role of the FRACTAL_NZ weight
+ *     cast in [W8A8] section 4.
+ *   - A zero-sized problem (M == 0, T == 0, rows == 0) returns FQ_OK
+ *     without launching anything ([PR] item 2: the wrapper skips the
+ *     launch when numel() == 0).
+ *   - Shape rules (else FQ_ERR_SHAPE): sizes >= 0; K % 16 == 0 and
+ *     N % 16 == 0 for int8 operands (the INT8 precheck K % 16, N % 32 of
+ *     [W8A8] section 4, relaxed to what TMA needs); D % 128 == 0 and
+ *     N % 128 == 0 for the FP8 path (whole 128-element groups / blocks).
+ *   - Workspace: calls that split K take a caller-owned device workspace of
+ *     at least fq_workspace_bytes(...) bytes.  It MUST be zero-filled once
+ *     before its first use (e.g. cudaMemsetAsync).  Its head holds per-tile
+ *     arrival counters that every completed call returns to zero; the rest
+ *     is scratch for split-K partial sums.  So a workspace is reused across
+ *     calls without clearing, but calls that may run concurrently
+ *     (different streams) must not share one, and after a call that
+ *     reported FQ_ERR_DEVICE_TIMEOUT it must be zero-filled again.
+ *   - Device-side problems that the host cannot see before launch (an
+ *     expert id out of range, a pipeline wait that ran out of time) are
+ *     recorded in a device error word and read with fq_device_error().
+ *   - The library needs an sm_103 device; anything else returns
+ *     FQ_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef FQ_H_
+#define FQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* fq_stream_t;
+
+typedef enum fq_status {
+  FQ_OK = 0,
+  FQ_ERR_NULL = 1,               /* a required pointer is NULL */
+  FQ_ERR_SHAPE = 2,              /* a size is negative, too large, or breaks a divisibility rule */
+  FQ_ERR_ALIGN = 3,              /* a pointer is not 16-byte aligned */
+  FQ_ERR_WORKSPACE = 4,          /* workspace missing or smaller than fq_workspace_bytes() */
+  FQ_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not sm_103 */
+  FQ_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed; see fq_last_cuda_error() */
+  FQ_ERR_DEVICE_TIMEOUT = 7,     /* a bounded device wait gave up (reported by fq_device_error) */
+  FQ_ERR_DEVICE_INPUT = 8,       /* device data broke the contract, e.g. expert id out of range */
+  FQ_ERR_ARG = 9                 /* an enum argument has an unknown value */
+} fq_status;
+
+/* Text for a status code; never NULL. */
+const char* fq_status_string(int status);
+
+/* The last CUDA error code seen by this thread inside the library (0 = none). */
+int fq_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns FQ_OK, FQ_ERR_DEVICE_TIMEOUT or
+ * FQ_ERR_DEVICE_INPUT; *detail (nullable) receives the raw word. */
+fq_status fq_device_error(fq_stream_t stream, uint32_t* detail);
+
+/* Workspace sizing.  `op` is one of fq_op; the four sizes are read as:
+ *   FQ_OP_W8A8_LINEAR, FQ_OP_W8A8_QUANT_LINEAR:   (M, K, N, unused)
+ *   FQ_OP_FP8_GROUP_EINSUM:                       (T, D, N, G)
+ *   FQ_OP_MOE_SORT:                               (T*topk, unused, unused, E)
+ *   FQ_OP_W8A8_GROUPED_LINEAR:                    (R rows, K, N, E)
+ * Returns 0 for an unknown op or invalid sizes. */
+typedef enum fq_op {
+  FQ_OP_W8A8_LINEAR = 1,
+  FQ_OP_W8A8_QUANT_LINEAR = 2,
+  FQ_OP_FP8_GROUP_EINSUM = 3,
+  FQ_OP_MOE_SORT = 4,
+  FQ_OP_W8A8_GROUPED_LINEAR = 5
+} fq_op;
+size_t fq_workspace_bytes(int op, int64_t a, int64_t b, int64_t c, int64_t d);
+
+/* ------------------------------------------------------------------ INT8 */
+
+/* Per-token INT8 dynamic quantization.
+ * [W8A8] section 1 (BF16 X -> npu_dynamic_quant -> INT8 X + per-token
+ * scale) and section 2 (a row is the last dimension; one token per row).
+ *   x  : bf16 [M, K]            in
+ *   xq : int8 [M, K]            out, q = clamp(rint(x / s), -127, 127), ties to even
+ *   sx : fp32 [M]               out, s = absmax(row) / 127 (IEEE fp32 division)
+ * An all-zero row gives s = 0 and q = 0. */
+fq_status dynamic_quant_int8(const uint16_t* x, int64_t M, int64_t K,
+                             int8_t* xq, float* sx, fq_stream_t stream);
+
+/* W8A8 linear on pre-quantized activations.
+ * [W8A8] section 1 (npu_quant_matmul -> BF16 Y; a linear may consume an
+ * upstream (int8, scale) tuple directly, skipping the quant).
+ *   xq   : int8 [M, K]   sx : fp32 [M]
+ *   w_nk : int8 [N, K] (K-major; logical W[k, n] = w_nk[n*K + k])
+ *   sw   : fp32 [N]      per-output-channel weight scale
+ *   y    : bf16 [M, N]   y = bf16_RN((fp32(acc) * sx[m]) * sw[n]),
+ *                        acc = exact int32 sum_k xq[m,k] * W[k,n]
+ *   ws   : workspace of fq_workspace_bytes(FQ_OP_W8A8_LINEAR, M, K, N, 0) bytes
+ * K <= 2^31 / (127*127) keeps acc inside int32. */
+fq_status w8a8_linear(const int8_t* xq, const float* sx, int64_t M, int64_t K,
+                      const int8_t* w_nk, const float* sw, int64_t N, uint16_t* y,
+                      void* ws, size_t ws_bytes, fq_stream_t stream);
+
+/* BF16 X -> per-token INT8 quant -> W8A8 linear, in one call.
+ * [W8A8] section 1: T_W8A8_linear = T_dynamic_quant + T_quant_matmul + ...
+ * Results are bit-identical to dynamic_quant_int8 followed by w8a8_linear.
+ *   xq_out, sx_out : nullable; when given they receive the quantized
+ *                    activations and scales (int8 [M, K], fp32 [M]).
+ *   ws : fq_workspace_bytes(FQ_OP_W8A8_QUANT_LINEAR, M, K, N, 0) bytes. */
+fq_status w8a8_quant_linear(const uint16_t* x, int64_t M, int64_t K,
+                            const int8_t* w_nk, const float* sw, int64_t N, uint16_t* y,
+                            int8_t* xq_out, float* sx_out,
+                            void* ws, size_t ws_bytes, fq_stream_t stream);
+
+/* ------------------------------------------------------------------- FP8 */
+
+/* FP8 E4M3 per-128-element group quant writing packed UE8M0 scales.
+ * [PR] implementation breakdown items 1-2 and the key source snippets.
+ *   x        : bf16 [T, G, D], D % 128 == 0       in
+ *   xq       : E4M3 [T, G, D]                     out
+ *   s_packed : int32 [G, P, Ta], P = ceil((D/128)/4), Ta = align_up(T, 4)  out
+ * For each (t, g, j) with j the 128-wide hidden group:
+ *   e = clamp(ceil(log2(absmax / 448)), -127, 127)   (absmax == 0 -> -127)
+ *   xq = E4M3_RN_satfinite(x * 2^-e)
+ *   byte (e + 127) at byte offset ((g*P + j/4)*Ta + t)*4 + j%4
+ * Every other byte of s_packed is written as zero: the bytes of the last
+ * pack past the last group (as in [PR]) and the token-padding words
+ * t in [T, Ta) (stronger than [PR], which leaves them uninitialised).
+ * The logical scale view is [T, G, P] with element strides (1, P*Ta, Ta). */
+fq_status quant_fp8_group_ue8m0_packed(const uint16_t* x, int64_t T, int64_t G, int64_t D,
+                                       uint8_t* xq, int32_t* s_packed, fq_stream_t stream);
+
+/* Same quant, writing unpacked fp32 scales 2^e as fp32 [T, G, D/128].
+ * This is the producer's form before the PR ([PR] motivation); kept as the
+ * A/B control together with fq_pack_scales_ue8m0. */
+fq_status quant_fp8_group_fp32(const uint16_t* x, int64_t T, int64_t G, int64_t D,
+                               uint8_t* xq, float* s_f32, fq_stream_t stream);
+
+/* fp32 power-of-two scales [T, G, NG] -> packed UE8M0 int32 [G, ceil(NG/4), align_up(T,4)],
+ * zero in the unused bytes and token padding.  The separate conversion
+ * ([PR] motivation: transpose_and_pack_fp32_into_ue8m0) that writing the
+ * packed layout directly removes.  Values that are not powers of two in
+ * [2^-127, 2^127] are outside the contract. */
+fq_status fq_pack_scales_ue8m0(const float* s_f32, int64_t T, int64_t G, int64_t NG,
+                               int32_t* s_packed, fq_stream_t stream);
+
+/* Load-time FP8 weight prep with fp32 per-128x128 block scales.
+ *   w_gnd : fp32 [G, N, D] (logical W[g, d, n] = w_gnd[(g*N + n)*D + d])
+ *   wq    : E4M3 [G, N, D]          wq = E4M3_RN_satfinite(fp32(w / sw_blk))
+ *   sw_blk: fp32 [G, D/128, N/128]  sw_blk = fp32(absmax(block) / 448)
+ * An all-zero block gives sw_blk = 0 and codes 0.  Untimed, offline step;
+ * the plain absmax reading of "fp32 per-128x128 block scales". */
+fq_status fq_quantize_weight_fp8_block(const float* w_gnd, int64_t G, int64_t N, int64_t D,
+                                       uint8_t* wq, float* sw_blk, fq_stream_t stream);
+
+typedef enum fq_scale_fmt {
+  FQ_SCALE_UE8M0_PACKED = 0, /* sx is int32 [G, ceil((D/128)/4), align_up(T,4)] (the producer's layout) */
+  FQ_SCALE_FP32 = 1          /* sx is fp32 [T, G, D/128] holding 2^e */
+} fq_scale_fmt;
+
+/* Block-scaled FP8 grouped einsum (the consumer of the packed scales).
+ * [PR] motivation / item 3: deep_gemm.fp8_einsum reading the TMA-aligned
+ * packed activation scales; the packed and fp32 scale paths must give
+ * bit-identical Y.
+ *   xq     : E4M3 [T, G, D]
+ *   sx     : scales in format `fmt`
+ *   w_gnd  : E4M3 [G, N, D] (logical W[g, d, n])
+ *   sw_blk : fp32 [G, D/128, N/128]
+ *   y      : bf16 [T, G, N]
+ *   Y[t,g,n] = bf16( sum_kb sx[t,g,kb] * sw[g,kb,n/128] * sum_{d in kb} xq[t,g,d] * W[g,d,n] )
+ * accumulated in fp32 with a fixed, data-independent order (deterministic).
+ *   ws : fq_workspace_bytes(FQ_OP_FP8_GROUP_EINSUM, T, D, N, G) bytes. */
+fq_status fp8_group_einsum(const uint8_t* xq, const void* sx, int fmt,
+                           int64_t T, int64_t G, int64_t D,
+                           const uint8_t* w_gnd, const float* sw_blk, int64_t N, uint16_t* y,
+                           void* ws, size_t ws_bytes, fq_stream_t stream);
+
+/* ------------------------------------------------------------------- MoE */
+
+/* Stable sort of the (token, slot) pairs of topk_ids [T, topk] by expert id.
+ * [DF] section 3.2 (sort tokens by expert id before dispatch so each
+ * expert's rows are contiguous) and [W8A8] section 5 (group_list =
+ * expert_tokens).
+ *   offsets  : int32 [E + 1]    out, exclusive scan of per-expert counts
+ *   perm     : int32 [T*topk]   out, perm[i] = flat pair index t*topk + j of sorted row i
+ *   pair_row : int32 [T*topk]   out (nullable), the inverse: sorted row of pair t*topk + j
+ * Ties keep pair order.  Ids outside [0, E) are dropped and flagged in the
+ * device error word (FQ_ERR_DEVICE_INPUT).  E <= 1024.
+ *   ws : fq_workspace_bytes(FQ_OP_MOE_SORT, T*topk, 0, 0, E) bytes. */
+fq_status moe_sort(const int32_t* topk_ids, int64_t T, int64_t topk, int64_t E,
+                   int32_t* offsets, int32_t* perm, int32_t* pair_row,
+                   void* ws, size_t ws_bytes, fq_stream_t stream);
+
+/* Gather of quantized token rows into expert order (the "gather" of
+ * [DF] section 3.2): row i of (xq_g, sx_g) is token perm[i] / topk of (xq, sx).
+ *   xq : int8 [T, K]  sx : fp32 [T]  ->  xq_g : int8 [R, K]  sx_g : fp32 [R], R = T*topk. */
+fq_status moe_gather_rows_i8(const int8_t* xq, const float* sx, const int32_t* perm,
+                             int64_t T, int64_t topk, int64_t K,
+                             int8_t* xq_g, float* sx_g, fq_stream_t stream);
+
+/* Grouped W8A8 linear: expert e multiplies rows [offsets[e], offsets[e+1])
+ * by its own weight.  [W8A8] section 5 (npu_grouped_matmul with
+ * group_list = expert_tokens; expert-local M_e).  Empty experts cost
+ * nothing.  Per row, exactly w8a8_linear with that expert's weight.
+ *   xq : int8 [R, K]  sx : fp32 [R]  offsets : int32 [E + 1] (device), offsets[E] == R
+ *   w_enk : int8 [E, N, K]   sw_en : fp32 [E, N]   y : bf16 [R, N]
+ *   ws : fq_workspace_bytes(FQ_OP_W8A8_GROUPED_LINEAR, R, K, N, E) bytes. */
+fq_status w8a8_grouped_linear(const int8_t* xq, const float* sx, const int32_t* offsets,
+                              int64_t R, int64_t E, int64_t K,
+                              const int8_t* w_enk, const float* sw_en, int64_t N, uint16_t* y,
+                              void* ws, size_t ws_bytes, fq_stream_t stream);
+
+/* SwiGLU fused with per-token INT8 re-quant.
+ * [DF] section 2.3 (activation fused with quantization, saving one write
+ * and read of the activation).
+ *   gu : bf16 [rows, 2*I]: gate g = columns [0, I), up u = columns [I, 2I)
+ *   h  = bf16_RN(fp32(silu(g)) * u), silu(g) = g / (1 + exp(-g)) in fp32
+ *   hq : int8 [rows, I], sh : fp32 [rows]  - dynamic_quant_int8 of h
+ *   h_out : bf16 [rows, I], nullable; receives h (for inspection). */
+fq_status swiglu_quant_int8(const uint16_t* gu, int64_t rows, int64_t I,
+                            int8_t* hq, float* sh, uint16_t* h_out, fq_stream_t stream);
+
+/* Weighted combine back to token order ([W8A8] section 1: T_combine).
+ *   y_rows   : bf16 [T*topk, H] in sorted (expert) order
+ *   pair_row : int32 [T*topk], sorted row of pair t*topk + j (from moe_sort)
+ *   topk_w   : fp32 [T, topk]
+ *   out[t]   = bf16_RN(running fp32 sum over j = 0..topk-1 of fp32(w[t,j] * y[pair_row[t*topk+j]]))
+ */
+fq_status moe_combine(const uint16_t* y_rows, const int32_t* pair_row, const float* topk_w,
+                      int64_t T, int64_t topk, int64_t H, uint16_t* out, fq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FQ_H_ */

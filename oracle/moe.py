@@ -68,7 +68,8 @@ def swiglu_bf16(gu_bf16):
     I = gu.shape[1] // 2
     g = gu[:, :I].astype(np.float64)
     u = gu[:, I:]
-    silu = (g / (1.0 + np.exp(-g))).astype(np.float32)
+    with np.errstate(over="ignore"):                    # exp(-g) = inf for g < -709: silu -> -0
+        silu = (g / (1.0 + np.exp(-g))).astype(np.float32)
     return f32_to_bf16((silu * u).astype(np.float32))
 
 
