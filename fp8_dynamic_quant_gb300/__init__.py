@@ -35,6 +35,7 @@ _SIGS = {
     "dynamic_quant_int8": ([_P, _I64, _I64, _P, _P, _P], _I32),
     "w8a8_linear": ([_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P], _I32),
     "w8a8_quant_linear": ([_P, _I64, _I64, _P, _P, _I64, _P, _P, _P, _P, _SZ, _P], _I32),
+    "w8a8_linear_noalloc": ([_P, _P, _I64, _I64, _P, _P, _I64, _P, _P], _I32),
     "quant_fp8_group_ue8m0_packed": ([_P, _I64, _I64, _I64, _P, _P, _P], _I32),
     "quant_fp8_group_fp32": ([_P, _I64, _I64, _I64, _P, _P, _P], _I32),
     "fq_pack_scales_ue8m0": ([_P, _I64, _I64, _I64, _P, _P], _I32),

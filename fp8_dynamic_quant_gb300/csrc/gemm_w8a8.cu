@@ -36,6 +36,8 @@
 //    issued before griddepcontrol.wait, overlapping the previous kernel.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "fq_common.cuh"
 
 namespace fq {
@@ -599,4 +601,72 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(
   if (!tw || !tx) return FQ_ERR_CUDA;
   return cuda_status(
       launch_gemm<mt, true>(tw, tx, p, d.sm_count, reinterpret_cast<cudaStream_t>(stream), pdl_enabled()));
+}
+
+// ================================================================ no-allocation variant
+//
+// w8a8_linear_noalloc: the same W8A8 linear for callers that cannot allocate
+// device memory - code running where cudaMalloc is unavailable or forbidden
+// (inside an allocator-free runtime, a plugin that must not touch the
+// caller's memory pool, or code that owns no device memory at all).  Its
+// split-K scratch is a fixed file-scope device array instead of a caller
+// workspace.
+namespace fq {
+namespace noalloc {
+constexpr int64_t kMaxM = 64;                                    // one token tile of 64
+constexpr int64_t kMaxTilesNA = 4096;                            // N <= 4096 * 128 = 524288
+constexpr int kMaxCtas = 160;                                    // one CTA per SM; GB300 has 152
+constexpr size_t kCountersNA = size_t(kMaxTilesNA) * 4;         // 16 KiB of arrival counters
+constexpr size_t kSlotsNA = size_t(2) * kMaxCtas * kBN * 64 * 4;  // 10 MiB of int32 partial sums
+constexpr size_t kScratchBytes = kCountersNA + kSlotsNA;
+}  // namespace noalloc
+
+// Held by every device that loads this library, for the life of the process.
+static __device__ __align__(256) uint8_t g_w8a8_noalloc_scratch[noalloc::kScratchBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[64] = {};
+
+// Device address of the scratch array on the current device (set-up once per
+// device, with that device current).  The host-side name of the array is only
+// a stand-in for the symbol and must never be passed to a kernel.
+static fq_status noalloc_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (dev < 0 || dev >= 64) return FQ_ERR_UNSUPPORTED_DEVICE;
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_w8a8_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return FQ_OK;
+}
+}  // namespace fq
+
+extern "C" __attribute__((visibility("default"))) fq_status w8a8_linear_noalloc(
+    const int8_t* xq, const float* sx, int64_t M, int64_t K, const int8_t* w_nk, const float* sw, int64_t N,
+    uint16_t* y, fq_stream_t stream) {
+  fq_status st = check_linear_args(M, K, N);
+  if (st != FQ_OK) return st;
+  if (M > noalloc::kMaxM) return FQ_ERR_SHAPE;
+  if (((N + kBN - 1) / kBN) > noalloc::kMaxTilesNA) return FQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return FQ_OK;
+  if (!xq || !sx || !w_nk || !sw || !y) return FQ_ERR_NULL;
+  if (!aligned16(xq) || !aligned16(sx) || !aligned16(w_nk) || !aligned16(sw) || !aligned16(y)) return FQ_ERR_ALIGN;
+  DevInfo d;
+  if ((st = device_info(&d)) != FQ_OK) return st;
+  if (d.sm_count > noalloc::kMaxCtas) return FQ_ERR_UNSUPPORTED_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(M) * size_t(N) * 2, s));
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(d.id, &scratch)) != FQ_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  const int64_t tiles = (N + kBN - 1) / kBN;  // M <= 64: one token tile
+  // The array keeps the previous call's contents: the arrival counters this
+  // call uses must start at zero.
+  cudaError_t e = cudaMemsetAsync(base, 0, size_t(tiles) * 4, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return run_w8a8_dense(xq, sx, M, K, w_nk, sw, N, y, reinterpret_cast<uint32_t*>(base), base + noalloc::kCountersNA,
+                        noalloc::kSlotsNA, s, d);
 }

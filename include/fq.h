@@ -135,6 +135,29 @@ fq_status w8a8_quant_linear(const uint16_t* x, int64_t M, int64_t K,
                             int8_t* xq_out, float* sx_out,
                             void* ws, size_t ws_bytes, fq_stream_t stream);
 
+/* W8A8 linear that allocates nothing - no counterpart in the pages.
+ * For callers that cannot allocate device memory: code that runs where
+ * cudaMalloc is unavailable or not allowed (an allocator-free runtime, a
+ * plugin that must not touch its host's memory pool), so that it cannot
+ * provide the workspace w8a8_linear needs.  Same arguments and bit-identical
+ * results as w8a8_linear, without the workspace.
+ *   Scratch: a fixed ~10.5 MB array in device memory (16 KiB of arrival
+ *   counters + 10 MiB of partial sums), reserved on every GPU that loads this
+ *   library and held until the process exits.
+ *   Limits: M <= 64, N <= 524288 (ceil(N/128) <= 4096 tiles), at most 160
+ *   SMs; larger sizes return FQ_ERR_SHAPE (FQ_ERR_UNSUPPORTED_DEVICE for more
+ *   SMs).  No cudaMalloc/cudaFree or allocating call is made.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.  Each call zeroes the counters it uses with
+ *   cudaMemsetAsync on `stream`, then launches the GEMM.
+ *   All calls share the one array: calls that may overlap on the GPU
+ *   (different streams, or different host threads) race and give wrong
+ *   results; serialise them. */
+fq_status w8a8_linear_noalloc(const int8_t* xq, const float* sx, int64_t M, int64_t K,
+                              const int8_t* w_nk, const float* sw, int64_t N, uint16_t* y,
+                              fq_stream_t stream);
+
 /* ------------------------------------------------------------------- FP8 */
 
 /* FP8 E4M3 per-128-element group quant writing packed UE8M0 scales.
