@@ -84,8 +84,29 @@ __device__ __forceinline__ float load_sx(const Problem& p, int t, int g, int kb)
   return __ldg(sf + (int64_t(t) * p.G + g) * p.KB + kb);
 }
 
-__device__ __forceinline__ int64_t range_begin(int64_t b, int64_t I, int64_t G) { return b * I / G; }
-__device__ __forceinline__ int64_t cta_of(int64_t i, int64_t I, int64_t G) { return ((i + 1) * G - 1) / I; }
+constexpr int kMaxGrid = 1024;
+// CTA whose stream-K range holds iteration i: the largest c with rb[c] <= i.
+__device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (rb[mid] <= i) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// tile = (g * NB + nb) * TT + tt
+struct ETile {
+  int g, nb, tt;
+};
+__device__ __forceinline__ ETile etile(const Problem& p, int tile) {
+  ETile t;
+  const int q = tile / p.TT;
+  t.tt = tile - q * p.TT;
+  t.g = q / p.NB;
+  t.nb = q - t.g * p.NB;
+  return t;
+}
 
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -100,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + S;
   __shared__ int s_flag, s_issued, s_consumed;
   __shared__ volatile int s_abort;
+  __shared__ int rb[kMaxGrid + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -116,50 +138,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
-  pdl_launch_dependents();
+  const int G = gridDim.x, b = blockIdx.x;
+  for (int c = tid; c <= G; c += kThreads) rb[c] = int(int64_t(c) * p.total / G);
   __syncthreads();
-
-  const int64_t I = p.total, Gd = gridDim.x, b = blockIdx.x;
-  const int64_t begin = range_begin(b, I, Gd), end = range_begin(b + 1, I, Gd);
+  const int begin = rb[b], end = rb[b + 1];
   const int KB = p.KB;
-  // tile = (g * NB + nb) * TT + tt
-  auto tile_w_row = [&](int64_t tile) { return int((tile / p.TT) / p.NB) * p.N + int((tile / p.TT) % p.NB) * kBN; };
 
   if (warp == kCW) {
     if (lane == 0 && end > begin) {
       const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-      const int64_t n_it = end - begin;
-      const int npre = int(n_it < S ? n_it : S);
-      for (int r = 0; r < npre; ++r) {
-        const int64_t it = begin + r;
-        mbar_arrive_expect_tx(&full[r], C::STAGE);
-        tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], int(it % KB) * kBK, tile_w_row(it / KB), pol_w);
+      const int n_it = end - begin;
+      const int npre = n_it < S ? n_it : S;
+      {
+        int tile = begin / KB, kb = begin - tile * KB;
+        ETile t = etile(p, tile);
+        for (int r = 0; r < npre; ++r) {
+          mbar_arrive_expect_tx(&full[r], C::STAGE);
+          tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], kb * kBK, t.g * p.N + t.nb * kBN, pol_w);
+          if (++kb == KB && r + 1 < npre) {
+            kb = 0;
+            t = etile(p, ++tile);
+          }
+        }
       }
       pdl_wait();
-      for (int r = 0; r < npre; ++r) {
-        const int64_t it = begin + r, tile = it / KB;
-        const int g = int((tile / p.TT) / p.NB), tt = int(tile % p.TT);
-        tma_load_2d(stages + r * C::STAGE + C::W_BYTES, &tmX, &full[r], g * p.D + int(it % KB) * kBK, tt * MT, pol_x);
-      }
-      int64_t issued = npre;
-      for (int64_t r = npre; r < n_it; ++r) {
-        const int s = int(r % S);
-        if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
-          if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
-          s_abort = 1;
-          break;
+      int tile = begin / KB, kb = begin - tile * KB;
+      ETile t = etile(p, tile);
+      int issued = 0;
+      for (int r = 0; r < n_it; ++r) {
+        const int s = r % S;
+        if (r < npre) {
+          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
+        } else {
+          if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
+            if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+            s_abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], kb * kBK, t.g * p.N + t.nb * kBN, pol_w);
+          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
         }
-        const int64_t it = begin + r, tile = it / KB;
-        const int g = int((tile / p.TT) / p.NB), tt = int(tile % p.TT);
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], int(it % KB) * kBK, tile_w_row(tile), pol_w);
-        tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], g * p.D + int(it % KB) * kBK, tt * MT, pol_x);
         ++issued;
+        if (++kb == KB && r + 1 < n_it) {
+          kb = 0;
+          t = etile(p, ++tile);
+        }
       }
-      s_issued = int(issued);
+      s_issued = issued;
     }
   } else {
     pdl_wait();
+    // Let the next kernel launch only once this one's inputs are final: a
+    // dependent may prefetch weights before its own wait, which is safe only
+    // if every earlier kernel has finished.
+    pdl_launch_dependents();
     const int gq = lane >> 2, c = lane & 3;
     float acc[NT][4];
 #pragma unroll
@@ -168,27 +201,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r < 4; ++r) acc[j][r] = 0.f;
     const uint32_t sbase = smem_u32(stages);
     const uint32_t rowW0 = uint32_t((16 * warp + gq) * kBK), rowW1 = rowW0 + 8 * kBK;
-    int64_t seg_kb0 = begin % KB;
+    int tile = begin / KB, kb = begin - tile * KB;
+    ETile t = etile(p, tile);
+    int seg_kb0 = kb;
     bool first_seg = true;
-    int64_t consumed = 0;
-    // scales of the current k-block (prefetched one iteration ahead)
+    int consumed = 0;
+    const int n_it = end - begin;
+    // scales of the current k-block, fetched one iteration ahead
     float sxv[NT][2], swv = 0.f;
-    auto fetch = [&](int64_t it, float out[NT][2], float& w) {
-      const int64_t tile = it / KB;
-      const int g = int((tile / p.TT) / p.NB), nb = int((tile / p.TT) % p.NB), tt = int(tile % p.TT);
-      const int kb = int(it % KB);
+    auto fetch = [&](const ETile& et, int k, float out[NT][2], float& w) {
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) out[j][h] = load_sx(p, tt * MT + 8 * j + 2 * c + h, g, kb);
-      w = __ldg(p.sw + (int64_t(g) * KB + kb) * p.NB + nb);
+        for (int h = 0; h < 2; ++h) out[j][h] = load_sx(p, et.tt * MT + 8 * j + 2 * c + h, et.g, k);
+      w = __ldg(p.sw + (int64_t(et.g) * KB + k) * p.NB + et.nb);
     };
-    if (end > begin) fetch(begin, sxv, swv);
-    for (int64_t it = begin; it < end; ++it) {
-      const int64_t r = it - begin;
-      const int s = int(r % S);
+    if (n_it > 0) fetch(t, kb, sxv, swv);
+    // position of the next iteration (for the scale prefetch)
+    int ntile = tile, nkb = kb;
+    ETile nt_ = t;
+    for (int r = 0; r < n_it; ++r) {
+      const int s = r % S;
       float nsx[NT][2], nsw = 0.f;
-      if (it + 1 < end) fetch(it + 1, nsx, nsw);
+      if (r + 1 < n_it) {
+        if (++nkb == KB) {
+          nkb = 0;
+          nt_ = etile(p, ++ntile);
+        }
+        fetch(nt_, nkb, nsx, nsw);
+      }
       bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
@@ -215,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                        word_of(wb, 2 * ks + 1), word_of(xv, 2 * ks), word_of(xv, 2 * ks + 1));
           }
         }
+        // The stage was read through the generic proxy (ld.shared); the next
+        // TMA write into it goes through the async proxy.  Order the two
+        // before handing the stage back, or TMA can overwrite it under the read.
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         ++consumed;
@@ -229,10 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sxv[j][1] = nsx[j][1];
       }
       swv = nsw;
-      const int kb = int(it % KB);
-      if (kb == KB - 1 || it == end - 1) {
-        const int64_t tile = it / KB;
-        const int g = int((tile / p.TT) / p.NB), nb = int((tile / p.TT) % p.NB), tt = int(tile % p.TT);
+      if (kb == KB - 1 || r == n_it - 1) {
         const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
         bool do_epi = whole;
         if (!whole) {
@@ -241,39 +283,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) my[((warp * NT + j) * 4 + rr) * 32 + lane] = acc[j][rr];
-          __threadfence();
           named_bar_sync(1, kCW * 32);
           if (tid == 0) {
             const uint32_t nbk = uint32_t(kb - seg_kb0 + 1);
-            const uint32_t old = atomicAdd(&p.counters[tile], nbk);
+            const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile], nbk);
             const int last = (old + nbk == uint32_t(KB)) ? 1 : 0;
-            if (last) {
-              __threadfence();
-              p.counters[tile] = 0;
-            }
+            if (last) p.counters[tile] = 0;
             s_flag = last;
           }
           named_bar_sync(1, kCW * 32);
           do_epi = s_flag != 0;
-          named_bar_sync(1, kCW * 32);  // s_flag is rewritten by the next segment
           if (do_epi) {
-            // fixed order: ascending CTA index, own partial at its place
-            const int64_t c0 = cta_of(tile * KB, I, Gd), c1 = cta_of(tile * KB + KB - 1, I, Gd);
+            // Fixed order: ascending CTA index over every contributor's slot
+            // (this CTA's own partial included, read back from its slot), so
+            // the fp32 sum does not depend on which CTA arrives last.
+            constexpr int U = NT <= 2 ? 8 : (NT <= 4 ? 4 : 2);
+            const int c0 = cta_of(rb, G, tile * KB), c1 = cta_of(rb, G, tile * KB + KB - 1);
             float tot[NT][4];
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
               for (int rr = 0; rr < 4; ++rr) tot[j][rr] = 0.f;
-            for (int64_t cc = c0; cc <= c1; ++cc) {
-              if (range_begin(cc + 1, I, Gd) == range_begin(cc, I, Gd)) continue;  // empty range: no partial
-              const int64_t first_tile = range_begin(cc, I, Gd) / KB;
-              const float* sl = p.slots + (2 * cc + (first_tile == tile ? 0 : 1)) * int64_t(C::SLOT);
+            for (int cb = c0; cb <= c1; cb += U) {
+              float v[U][NT][4];
+              bool use[U];
 #pragma unroll
-              for (int j = 0; j < NT; ++j)
+              for (int u = 0; u < U; ++u) {
+                const int cc = cb + u;
+                use[u] = cc <= c1 && rb[cc + 1] != rb[cc];
+                const int first_tile = use[u] ? rb[cc] / KB : 0;
+                const float* sl = p.slots + (2 * int64_t(cc) + (first_tile == tile ? 0 : 1)) * int64_t(C::SLOT);
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                  const float v = (cc == b) ? acc[j][rr] : __ldcg(sl + ((warp * NT + j) * 4 + rr) * 32 + lane);
-                  tot[j][rr] = __fadd_rn(tot[j][rr], v);
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                  for (int rr = 0; rr < 4; ++rr)
+                    v[u][j][rr] = use[u] ? __ldcg(sl + ((warp * NT + j) * 4 + rr) * 32 + lane) : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+                if (use[u]) {
+#pragma unroll
+                  for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) tot[j][rr] = __fadd_rn(tot[j][rr], v[u][j][rr]);
                 }
             }
 #pragma unroll
@@ -281,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int rr = 0; rr < 4; ++rr) acc[j][rr] = tot[j][rr];
           }
+          named_bar_sync(1, kCW * 32);  // s_flag is rewritten by the next segment
         }
         if (do_epi) {
 #pragma unroll
@@ -292,13 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               epi[ml * kBN + nl] = f32_to_bf16_bits(acc[j][rr]);
             }
           named_bar_sync(1, kCW * 32);
-          const int n0 = nb * kBN;
+          const int n0 = t.nb * kBN;
           for (int idx = tid; idx < MT * (kBN / 8); idx += kCW * 32) {
             const int ml = idx / (kBN / 8), c8 = idx % (kBN / 8);
-            const int t = tt * MT + ml;
-            if (t < p.T) {
+            const int tok = t.tt * MT + ml;
+            if (tok < p.T) {
               const uint4 v = *reinterpret_cast<const uint4*>(epi + ml * kBN + c8 * 8);
-              *reinterpret_cast<uint4*>(p.y + (int64_t(t) * p.G + g) * p.N + n0 + c8 * 8) = v;
+              *reinterpret_cast<uint4*>(p.y + (int64_t(tok) * p.G + t.g) * p.N + n0 + c8 * 8) = v;
             }
           }
           named_bar_sync(1, kCW * 32);
@@ -310,12 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_seg = false;
         seg_kb0 = 0;
       }
+      if (++kb == KB) {
+        kb = 0;
+        t = etile(p, ++tile);
+      }
     }
-    if (tid == 0) s_consumed = int(consumed);
+    if (tid == 0) s_consumed = consumed;
   }
   __syncthreads();
   if (tid == 0) {
-    for (int64_t r = s_consumed; r < s_issued; ++r) mbar_wait(&full[int(r % S)], uint32_t((r / S) & 1));
+    for (int r = s_consumed; r < s_issued; ++r) mbar_wait(&full[r % S], uint32_t((r / S) & 1));
   }
 }
 

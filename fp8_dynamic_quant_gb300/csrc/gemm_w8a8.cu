@@ -116,10 +116,10 @@ struct TileCoord {
 };
 
 template <int MT, bool GROUPED>
-__device__ __forceinline__ TileCoord decode_tile(const Problem& p, int64_t tile, const int* tile_start) {
+__device__ __forceinline__ TileCoord decode_tile(const Problem& p, int tile, const int* tile_start) {
   TileCoord tc;
   if (!GROUPED) {
-    const int nt = int(tile / p.m_tiles), mt = int(tile % p.m_tiles);
+    const int nt = tile / p.m_tiles, mt = tile - nt * p.m_tiles;
     tc.w_row = nt * kBN;
     tc.n0 = nt * kBN;
     tc.x_row = mt * MT;
@@ -135,7 +135,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Problem& p, int64_t tile,
     const int e = lo;
     const int r0 = p.offsets[e], me = p.offsets[e + 1] - r0;
     const int mtn = (me + MT - 1) / MT;
-    const int local = int(tile - tile_start[e]);
+    const int local = tile - tile_start[e];
     const int nt = local / mtn, mt = local % mtn;
     tc.w_row = e * p.N + nt * kBN;
     tc.n0 = nt * kBN;
@@ -146,9 +146,18 @@ __device__ __forceinline__ TileCoord decode_tile(const Problem& p, int64_t tile,
   return tc;
 }
 
-__device__ __forceinline__ int64_t range_begin(int64_t b, int64_t I, int64_t G) { return b * I / G; }
-// CTA whose range holds iteration i: the largest b with floor(b*I/G) <= i.
-__device__ __forceinline__ int64_t cta_of(int64_t i, int64_t I, int64_t G) { return ((i + 1) * G - 1) / I; }
+// Stream-K ranges: CTA b owns iterations [rb[b], rb[b+1]) with
+// rb[b] = floor(b * I / G), tabulated once per CTA in shared memory.
+constexpr int kMaxGrid = 1024;
+// CTA whose range holds iteration i: the largest c with rb[c] <= i (rb ascending, rb[0] = 0).
+__device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
+  int lo = 0, hi = G;  // rb[lo] <= i < rb[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (rb[mid] <= i) lo = mid; else hi = mid;
+  }
+  return lo;
+}
 
 // ---------------------------------------------------------------- the kernel
 template <int MT, bool GROUPED>
@@ -166,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_issued, s_consumed;
   __shared__ volatile int s_abort;  // set after any timed-out wait: later waits are skipped
   __shared__ int tile_start_s[GROUPED ? 1025 : 1];
+  __shared__ int rb[kMaxGrid + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -182,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
-  pdl_launch_dependents();
 
   int64_t I = p.total;
   if (GROUPED) {
@@ -223,53 +232,64 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  const int64_t G = gridDim.x, b = blockIdx.x;
-  const int64_t begin = range_begin(b, I, G), end = range_begin(b + 1, I, G);
+  const int G = gridDim.x, b = blockIdx.x;
+  for (int c = tid; c <= G; c += kThreads) rb[c] = int(int64_t(c) * I / G);
+  __syncthreads();
+  const int begin = rb[b], end = rb[b + 1];
   const int KB = p.KB;
 
   if (warp == kCW) {
     // ------------------------------------------------ producer warp
     if (lane == 0 && end > begin) {
       const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-      const int64_t n_it = end - begin;
-      const int npre = int(n_it < S ? n_it : S);
-      bool ok = true;
+      const int n_it = end - begin;
+      const int npre = n_it < S ? n_it : S;
       // weights do not depend on the previous kernel: issue them first
-      for (int r = 0; r < npre; ++r) {
-        const int64_t it = begin + r;
-        const TileCoord tc = decode_tile<MT, GROUPED>(p, it / KB, tile_start_s);
-        mbar_arrive_expect_tx(&full[r], C::STAGE);
-        tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], int(it % KB) * kBK, tc.w_row, pol_w);
+      {
+        int tile = begin / KB, kb = begin - tile * KB;
+        TileCoord tc = decode_tile<MT, GROUPED>(p, tile, tile_start_s);
+        for (int r = 0; r < npre; ++r) {
+          mbar_arrive_expect_tx(&full[r], C::STAGE);
+          tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], kb * kBK, tc.w_row, pol_w);
+          if (++kb == KB && r + 1 < npre) {
+            kb = 0;
+            tc = decode_tile<MT, GROUPED>(p, ++tile, tile_start_s);
+          }
+        }
       }
       pdl_wait();
-      for (int r = 0; r < npre; ++r) {
-        const int64_t it = begin + r;
-        const TileCoord tc = decode_tile<MT, GROUPED>(p, it / KB, tile_start_s);
-        tma_load_2d(stages + r * C::STAGE + C::W_BYTES, &tmX, &full[r], int(it % KB) * kBK, tc.x_row, pol_x);
-      }
-      int64_t issued = npre;
-      for (int64_t r = npre; r < n_it; ++r) {
-        const int s = int(r % S);
-        const uint32_t ph = uint32_t((r / S - 1) & 1);
-        if (s_abort || !mbar_wait(&empty[s], ph)) {
-          if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
-          s_abort = 1;
-          ok = false;
-          break;
+      int tile = begin / KB, kb = begin - tile * KB;
+      TileCoord tc = decode_tile<MT, GROUPED>(p, tile, tile_start_s);
+      int issued = 0;
+      for (int r = 0; r < n_it; ++r) {
+        const int s = r % S;
+        if (r < npre) {
+          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
+        } else {
+          if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
+            if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+            s_abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], kb * kBK, tc.w_row, pol_w);
+          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
         }
-        const int64_t it = begin + r;
-        const TileCoord tc = decode_tile<MT, GROUPED>(p, it / KB, tile_start_s);
-        mbar_arrive_expect_tx(&full[s], C::STAGE);
-        tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], int(it % KB) * kBK, tc.w_row, pol_w);
-        tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], int(it % KB) * kBK, tc.x_row, pol_x);
         ++issued;
+        if (++kb == KB && r + 1 < n_it) {
+          kb = 0;
+          tc = decode_tile<MT, GROUPED>(p, ++tile, tile_start_s);
+        }
       }
-      (void)ok;
-      s_issued = int(issued);
+      s_issued = issued;
     }
   } else {
     // ------------------------------------------------ consumer warps
     pdl_wait();
+    // Let the next kernel launch only once this one's inputs are final: a
+    // dependent may prefetch weights before its own wait, which is safe only
+    // if every earlier kernel has finished.
+    pdl_launch_dependents();
     const int g = lane >> 2, c = lane & 3;
     float accf[NT][4];
     int acci[NT][4];
@@ -282,15 +302,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     const uint32_t sbase = smem_u32(stages);
     const uint32_t rowW0 = uint32_t((16 * warp + g) * kBK), rowW1 = rowW0 + 8 * kBK;
-    int64_t seg_kb0 = begin % KB;
+    int tile = begin / KB, kb = begin - tile * KB;
+    int seg_kb0 = kb;
     int nk = 0;
     bool first_seg = true;
-    int64_t consumed = 0;
+    int consumed = 0;
+    const int n_it = end - begin;
+    // Dequant scales of the current tile, loaded when its segment starts so the
+    // epilogue does not wait on a global round trip.
+    float sxr[NT][2], swr[2];
+    auto load_scales = [&](int t) {
+      const TileCoord tc = decode_tile<MT, GROUPED>(p, t, tile_start_s);
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int ml = 8 * j + 2 * c + h;
+          sxr[j][h] = ml < tc.rows ? __ldg(p.sx + tc.x_row + ml) : 0.f;
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int n = tc.n0 + 16 * warp + g + 8 * h;
+        swr[h] = n < p.N ? __ldg(p.sw + tc.sw_base + n) : 0.f;
+      }
+    };
+    if (n_it > 0) load_scales(tile);
     // After a timeout (s_abort) the loop keeps its shape - same segments, same
     // named barriers - but skips waits and math, so every warp finishes.
-    for (int64_t it = begin; it < end; ++it) {
-      const int64_t r = it - begin;
-      const int s = int(r % S);
+    for (int r = 0; r < n_it; ++r) {
+      const int s = r % S;
       bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
@@ -318,13 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // The stage was read through the generic proxy (ld.shared); the next
+      // TMA write into it goes through the async proxy.  Order the two before
+      // handing the stage back, or TMA can overwrite it under the read.
+      fence_proxy_async_smem();
       __syncwarp();
       if (ok) {
         if (lane == 0) mbar_arrive(&empty[s]);
         ++consumed;
       }
-      const int kb = int(it % KB);
-      if (++nk == kFlushBlocks || kb == KB - 1 || it == end - 1) {
+      const bool seg_end = (kb == KB - 1) || (r == n_it - 1);
+      if (++nk == kFlushBlocks || seg_end) {
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -334,9 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         nk = 0;
       }
-      if (kb == KB - 1 || it == end - 1) {
-        // ---- segment end: tile (it / KB), k-blocks [seg_kb0, kb]
-        const int64_t tile = it / KB;
+      if (seg_end) {
+        // ---- segment end: tile `tile`, k-blocks [seg_kb0, kb]
         const TileCoord tc = decode_tile<MT, GROUPED>(p, tile, tile_start_s);
         const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
         bool do_epi = whole;
@@ -346,31 +389,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) my[((warp * NT + j) * 4 + rr) * 32 + lane] = acci[j][rr];
-          __threadfence();
           named_bar_sync(1, kCW * 32);
           if (tid == 0) {
             const uint32_t nb = uint32_t(kb - seg_kb0 + 1);
-            const uint32_t old = atomicAdd(&p.counters[tile], nb);
+            const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile], nb);
             const int last = (old + nb == uint32_t(KB)) ? 1 : 0;
-            if (last) {
-              __threadfence();
-              p.counters[tile] = 0;  // every contributor has arrived; ready for the next call
-            }
+            if (last) p.counters[tile] = 0;  // every contributor has arrived; ready for the next call
             s_flag = last;
           }
           named_bar_sync(1, kCW * 32);
           do_epi = s_flag != 0;
           if (do_epi) {
-            const int64_t c0 = cta_of(tile * KB, I, G), c1 = cta_of(tile * KB + KB - 1, I, G);
-            for (int64_t cc = c0; cc <= c1; ++cc) {
-              // CTAs with an empty range (more CTAs than iterations) wrote nothing
-              if (cc == b || range_begin(cc + 1, I, G) == range_begin(cc, I, G)) continue;
-              const int64_t first_tile = range_begin(cc, I, G) / KB;
-              const int32_t* sl = p.slots + (2 * cc + (first_tile == tile ? 0 : 1)) * int64_t(C::SLOT);
+            // add the other contributors' partials; U slots in flight at once
+            constexpr int U = NT <= 2 ? 8 : (NT <= 4 ? 4 : 2);
+            const int c0 = cta_of(rb, G, tile * KB), c1 = cta_of(rb, G, tile * KB + KB - 1);
+            for (int cb = c0; cb <= c1; cb += U) {
+              int32_t v[U][NT][4];
 #pragma unroll
-              for (int j = 0; j < NT; ++j)
+              for (int u = 0; u < U; ++u) {
+                const int cc = cb + u;
+                // skip self and CTAs with an empty range (more CTAs than iterations)
+                const bool use = cc <= c1 && cc != b && rb[cc + 1] != rb[cc];
+                const int first_tile = use ? rb[cc] / KB : 0;
+                const int32_t* sl = p.slots + (2 * int64_t(cc) + (first_tile == tile ? 0 : 1)) * int64_t(C::SLOT);
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) acci[j][rr] += __ldcg(sl + ((warp * NT + j) * 4 + rr) * 32 + lane);
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                  for (int rr = 0; rr < 4; ++rr)
+                    v[u][j][rr] = use ? __ldcg(sl + ((warp * NT + j) * 4 + rr) * 32 + lane) : 0;
+              }
+#pragma unroll
+              for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                  for (int rr = 0; rr < 4; ++rr) acci[j][rr] += v[u][j][rr];
             }
           }
         }
@@ -384,16 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int ml = 8 * j + 2 * c + (rr & 1);
               const int n = tc.n0 + nl;
               float v = 0.f;
-              if (ml < tc.rows && n < p.N) {
-                const float sxv = p.sx[tc.x_row + ml];
-                const float swv = p.sw[tc.sw_base + n];
-                v = __fmul_rn(__fmul_rn(__int2float_rn(acci[j][rr]), sxv), swv);
-              }
+              if (ml < tc.rows && n < p.N)
+                v = __fmul_rn(__fmul_rn(__int2float_rn(acci[j][rr]), sxr[j][rr & 1]), swr[rr >> 1]);
               epi[ml * kBN + nl] = f32_to_bf16_bits(v);
             }
           named_bar_sync(1, kCW * 32);
-          const int ctid = tid;  // 0..255
-          for (int idx = ctid; idx < MT * (kBN / 8); idx += kCW * 32) {
+          for (int idx = tid; idx < MT * (kBN / 8); idx += kCW * 32) {
             const int ml = idx / (kBN / 8), c8 = idx % (kBN / 8);
             const int n = tc.n0 + c8 * 8;
             if (ml < tc.rows && n < p.N) {
@@ -410,14 +459,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_seg = false;
         seg_kb0 = 0;
       }
+      if (++kb == KB) {
+        kb = 0;
+        ++tile;
+        if (r + 1 < n_it) load_scales(tile);
+      }
     }
-    if (tid == 0) s_consumed = int(consumed);
+    if (tid == 0) s_consumed = consumed;
   }
   __syncthreads();
   // Drain: on the normal path every issued stage was consumed.  After a
   // timeout, wait (bounded) for copies still in flight before exiting.
   if (tid == 0) {
-    for (int64_t r = s_consumed; r < s_issued; ++r) mbar_wait(&full[int(r % S)], uint32_t((r / S) & 1));
+    for (int r = s_consumed; r < s_issued; ++r) mbar_wait(&full[r % S], uint32_t((r / S) & 1));
   }
 }
 

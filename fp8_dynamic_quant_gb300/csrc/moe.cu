@@ -29,8 +29,8 @@ __global__ void __launch_bounds__(kSortWarps * 32) moe_sort_kernel(const int32_t
   int* cnt = smem;                       // [kSortWarps][E] counts, then cursors
   int* tot = smem + kSortWarps * E;      // [E + 1] totals, then offsets
   __shared__ int wsum[32];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < kSortWarps * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kSortWarps * 32) moe_sort_kernel(const int32_t
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ pair_row,
                                                           const float* __restrict__ w, int T, int topk, int H8,
                                                           int R, uint4* __restrict__ out, uint32_t* __restrict__ err) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const int c = blockIdx.y * blockDim.x + threadIdx.x;
   if (t >= T || c >= H8) return;

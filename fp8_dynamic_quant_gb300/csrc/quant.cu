@@ -99,8 +99,8 @@ __global__ void __launch_bounds__(256) dynamic_quant_int8_kernel(const uint4* __
                                                                   int64_t K8, uint2* __restrict__ q,
                                                                   float* __restrict__ s) {
   __shared__ float red[32];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x, nt = blockDim.x;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const uint4* xr = x + row * K8;
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(256) swiglu_quant_int8_kernel(const uint4* __r
                                                                  int64_t I8, uint2* __restrict__ hq,
                                                                  float* __restrict__ sh, uint4* __restrict__ hout) {
   __shared__ float red[32];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x, nt = blockDim.x;
   for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const uint4* gr = gu + row * 2 * I8;
@@ -229,8 +229,8 @@ __global__ void __launch_bounds__(256) gather_rows_i8_kernel(const uint4* __rest
                                                               const int32_t* __restrict__ perm, int64_t R,
                                                               int64_t topk, int64_t K16, int64_t T,
                                                               uint4* __restrict__ xg, float* __restrict__ sg) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int64_t row = int64_t(blockIdx.x) * warps + warp; row < R; row += int64_t(gridDim.x) * warps) {
     int64_t src = perm[row] / topk;
@@ -277,8 +277,8 @@ __global__ void __launch_bounds__(256) quant_fp8_group_kernel(const uint4* __res
                                                                int P, int Ta, uint4* __restrict__ xq,
                                                                int32_t* __restrict__ s_packed,
                                                                float* __restrict__ s_f32) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane >> 3, l8 = lane & 7;
   const int64_t D16 = int64_t(NG) * 16;  // 16-byte vectors of bf16 per (t, g) row (8 elem each)
@@ -333,8 +333,8 @@ __global__ void __launch_bounds__(256) quant_fp8_group_kernel(const uint4* __res
 // fp32 power-of-two scales [T, G, NG] -> packed int32 [G, P, Ta]; one thread per word.
 __global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restrict__ s, int T, int G, int NG, int P,
                                                            int Ta, int32_t* __restrict__ out) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t words = int64_t(G) * P * Ta;
   for (int64_t w = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; w < words; w += int64_t(gridDim.x) * blockDim.x) {
     const int t = int(w % Ta);
