@@ -85,6 +85,11 @@ __device__ __forceinline__ float load_sx(const Problem& p, int t, int g, int kb)
 }
 
 constexpr int kMaxGrid = 1024;
+
+// Fragment row g (0..7) of a 16-row block reads shared-memory row R(g), so the
+// two rows of each quarter-warp phase of a 16-byte ld.shared fall in different
+// halves of the 128-byte swizzle atom (conflict-free).
+__device__ __forceinline__ int frag_row(int g) { return (g >> 1) | ((g & 1) << 2); }
 // CTA whose stream-K range holds iteration i: the largest c with rb[c] <= i.
 __device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
   int lo = 0, hi = G;
@@ -194,13 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // if every earlier kernel has finished.
     pdl_launch_dependents();
     const int gq = lane >> 2, c = lane & 3;
+    const int rg = frag_row(gq);
     float acc[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[j][r] = 0.f;
     const uint32_t sbase = smem_u32(stages);
-    const uint32_t rowW0 = uint32_t((16 * warp + gq) * kBK), rowW1 = rowW0 + 8 * kBK;
+    const uint32_t rowW0 = uint32_t((16 * warp + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
     int tile = begin / KB, kb = begin - tile * KB;
     ETile t = etile(p, tile);
     int seg_kb0 = kb;
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) out[j][h] = load_sx(p, et.tt * MT + 8 * j + 2 * c + h, et.g, k);
+        for (int h = 0; h < 2; ++h) out[j][h] = load_sx(p, et.tt * MT + 8 * j + frag_row(2 * c + h), et.g, k);
       w = __ldg(p.sw + (int64_t(et.g) * KB + k) * p.NB + et.nb);
     };
     if (n_it > 0) fetch(t, kb, sxv, swv);
@@ -237,24 +243,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         const uint32_t st = sbase + uint32_t(s * C::STAGE);
-        float blk[NT][4];
+        // one fp32 chain per 64-byte half when there are few token tiles
+        constexpr int NB2 = NT <= 2 ? 2 : 1;
+        float blk[NB2][NT][4];
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+        for (int a = 0; a < NB2; ++a)
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) blk[j][rr] = 0.f;
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) blk[a][j][rr] = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t q = uint32_t(((4 * h + c) ^ gq) << 4);
+          const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
           const uint4 wa = lds128(st + rowW0 + q);
           const uint4 wb = lds128(st + rowW1 + q);
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            const uint4 xv = lds128(st + C::W_BYTES + uint32_t((8 * j + gq) * kBK) + q);
+            const uint4 xv = lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q);
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks)
-              mma_e4m3(blk[j], word_of(wa, 2 * ks), word_of(wb, 2 * ks), word_of(wa, 2 * ks + 1),
+              mma_e4m3(blk[h % NB2][j], word_of(wa, 2 * ks), word_of(wb, 2 * ks), word_of(wa, 2 * ks + 1),
                        word_of(wb, 2 * ks + 1), word_of(xv, 2 * ks), word_of(xv, 2 * ks + 1));
           }
+        }
+        if (NB2 == 2) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) blk[0][j][rr] = __fadd_rn(blk[0][j][rr], blk[NB2 - 1][j][rr]);
         }
         // The stage was read through the generic proxy (ld.shared); the next
         // TMA write into it goes through the async proxy.  Order the two
@@ -266,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) acc[j][rr] = __fmaf_rn(blk[j][rr], __fmul_rn(sxv[j][rr & 1], swv), acc[j][rr]);
+          for (int rr = 0; rr < 4; ++rr) acc[j][rr] = __fmaf_rn(blk[0][j][rr], __fmul_rn(sxv[j][rr & 1], swv), acc[j][rr]);
       }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
@@ -340,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
-              const int nl = 16 * warp + gq + ((rr & 2) ? 8 : 0);
-              const int ml = 8 * j + 2 * c + (rr & 1);
+              const int nl = 16 * warp + rg + ((rr & 2) ? 8 : 0);
+              const int ml = 8 * j + frag_row(2 * c + (rr & 1));
               epi[ml * kBN + nl] = f32_to_bf16_bits(acc[j][rr]);
             }
           named_bar_sync(1, kCW * 32);

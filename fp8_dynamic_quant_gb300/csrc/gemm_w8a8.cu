@@ -42,23 +42,35 @@
 
 namespace fq {
 
-constexpr int kBN = 128;             // weight rows (channels) per tile
 constexpr int kBK = 128;             // K bytes per k-block
-constexpr int kCW = 8;               // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;
 constexpr int kFlushBlocks = 8;      // fold fp32 -> int32 every 8 k-blocks (1024 K)
+constexpr int kBN = 128;             // weight rows per tile in the stream-K configuration (8 consumer warps)
 
-template <int MT>
+// MT tokens per tile, CW consumer warps of 16 weight rows each (BN = 16 * CW
+// rows per tile), plus one producer warp.
+template <int MT, int CW>
 struct Cfg {
   static constexpr int NT = MT / 8;
-  static constexpr int W_BYTES = kBN * kBK;
+  static constexpr int BN = 16 * CW;
+  static constexpr int THREADS = (CW + 1) * 32;
+  static constexpr int W_BYTES = BN * kBK;
   static constexpr int X_BYTES = MT * kBK;
   static constexpr int STAGE = W_BYTES + X_BYTES;           // multiple of 1024
-  static constexpr int STAGES = MT <= 16 ? 8 : 6;
-  static constexpr int EPI = kBN * MT * 2;                  // bf16 staging
-  static constexpr int SLOT = kBN * MT;                     // int32 per slot
+  static constexpr int EPI = BN * MT * 2;                   // bf16 staging
+  static constexpr int SMEM_BUDGET = 200 * 1024;
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - EPI - 2048) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SLOT = BN * MT;                      // int32 per slot
   static constexpr int SMEM = STAGES * STAGE + EPI + 2 * STAGES * 8 + 64 + 1024;  // + alignment slack
+  static_assert(STAGES >= 3, "pipeline too shallow");
 };
+
+// Fragment row g (0..7) of a 16-row block reads shared-memory row R(g).  The
+// 128-byte TMA swizzle XORs the 16-byte chunk index with (row & 7); with this
+// permutation the two rows served in one quarter-warp phase of a 16-byte
+// ld.shared (g = 2k, 2k+1) land in different 64-byte halves, so every phase
+// touches all 32 banks once.
+__device__ __forceinline__ int frag_row(int g) { return (g >> 1) | ((g & 1) << 2); }
 
 struct Problem {
   int M, N, K, KB;          // tokens (dense) / rows (grouped), channels, depth, k-blocks
@@ -115,13 +127,13 @@ struct TileCoord {
   int sw_base;   // offset of this tile's expert in sw
 };
 
-template <int MT, bool GROUPED>
+template <int MT, int BN, bool GROUPED>
 __device__ __forceinline__ TileCoord decode_tile(const Problem& p, int tile, const int* tile_start) {
   TileCoord tc;
   if (!GROUPED) {
     const int nt = tile / p.m_tiles, mt = tile - nt * p.m_tiles;
-    tc.w_row = nt * kBN;
-    tc.n0 = nt * kBN;
+    tc.w_row = nt * BN;
+    tc.n0 = nt * BN;
     tc.x_row = mt * MT;
     tc.rows = min(MT, p.M - mt * MT);
     tc.sw_base = 0;
@@ -137,8 +149,8 @@ __device__ __forceinline__ TileCoord decode_tile(const Problem& p, int tile, con
     const int mtn = (me + MT - 1) / MT;
     const int local = tile - tile_start[e];
     const int nt = local / mtn, mt = local % mtn;
-    tc.w_row = e * p.N + nt * kBN;
-    tc.n0 = nt * kBN;
+    tc.w_row = e * p.N + nt * BN;
+    tc.n0 = nt * BN;
     tc.x_row = r0 + mt * MT;
     tc.rows = min(MT, me - mt * MT);
     tc.sw_base = e * p.N;
@@ -160,11 +172,11 @@ __device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int MT, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MT, int CW, bool GROUPED>
+__global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
-  using C = Cfg<MT>;
-  constexpr int NT = C::NT, S = C::STAGES;
+  using C = Cfg<MT, CW>;
+  constexpr int NT = C::NT, S = C::STAGES, BN = C::BN, kThreads = C::THREADS, kCW = CW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -247,19 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weights do not depend on the previous kernel: issue them first
       {
         int tile = begin / KB, kb = begin - tile * KB;
-        TileCoord tc = decode_tile<MT, GROUPED>(p, tile, tile_start_s);
+        TileCoord tc = decode_tile<MT, BN, GROUPED>(p, tile, tile_start_s);
         for (int r = 0; r < npre; ++r) {
           mbar_arrive_expect_tx(&full[r], C::STAGE);
           tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], kb * kBK, tc.w_row, pol_w);
           if (++kb == KB && r + 1 < npre) {
             kb = 0;
-            tc = decode_tile<MT, GROUPED>(p, ++tile, tile_start_s);
+            tc = decode_tile<MT, BN, GROUPED>(p, ++tile, tile_start_s);
           }
         }
       }
       pdl_wait();
       int tile = begin / KB, kb = begin - tile * KB;
-      TileCoord tc = decode_tile<MT, GROUPED>(p, tile, tile_start_s);
+      TileCoord tc = decode_tile<MT, BN, GROUPED>(p, tile, tile_start_s);
       int issued = 0;
       for (int r = 0; r < n_it; ++r) {
         const int s = r % S;
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++issued;
         if (++kb == KB && r + 1 < n_it) {
           kb = 0;
-          tc = decode_tile<MT, GROUPED>(p, ++tile, tile_start_s);
+          tc = decode_tile<MT, BN, GROUPED>(p, ++tile, tile_start_s);
         }
       }
       s_issued = issued;
@@ -291,17 +303,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // if every earlier kernel has finished.
     pdl_launch_dependents();
     const int g = lane >> 2, c = lane & 3;
-    float accf[NT][4];
+    const int rg = frag_row(g);
+    // With few token tiles, two fp32 chains (even / odd 64-byte halves of a
+    // k-block) halve the dependent-MMA latency; both fold into the exact int32
+    // sum.  With NT >= 4 the token tiles already give independent chains.
+    constexpr int NACC = NT <= 2 ? 2 : 1;
+    float accf[NACC][NT][4];
     int acci[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        accf[j][r] = 0.f;
+#pragma unroll
+        for (int a = 0; a < NACC; ++a) accf[a][j][r] = 0.f;
         acci[j][r] = 0;
       }
     const uint32_t sbase = smem_u32(stages);
-    const uint32_t rowW0 = uint32_t((16 * warp + g) * kBK), rowW1 = rowW0 + 8 * kBK;
+    const uint32_t rowW0 = uint32_t((16 * warp + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
     int tile = begin / KB, kb = begin - tile * KB;
     int seg_kb0 = kb;
     int nk = 0;
@@ -312,17 +330,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue does not wait on a global round trip.
     float sxr[NT][2], swr[2];
     auto load_scales = [&](int t) {
-      const TileCoord tc = decode_tile<MT, GROUPED>(p, t, tile_start_s);
+      const TileCoord tc = decode_tile<MT, BN, GROUPED>(p, t, tile_start_s);
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int ml = 8 * j + 2 * c + h;
+          const int ml = 8 * j + frag_row(2 * c + h);
           sxr[j][h] = ml < tc.rows ? __ldg(p.sx + tc.x_row + ml) : 0.f;
         }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int n = tc.n0 + 16 * warp + g + 8 * h;
+        const int n = tc.n0 + 16 * warp + rg + 8 * h;
         swr[h] = n < p.N ? __ldg(p.sw + tc.sw_base + n) : 0.f;
       }
     };
@@ -339,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = sbase + uint32_t(s * C::STAGE);
 #pragma unroll
       for (int h = 0; h < 2 && ok; ++h) {
-        const uint32_t q = uint32_t(((4 * h + c) ^ g) << 4);
+        const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
         const uint4 wa = lds128(st + rowW0 + q);
         const uint4 wb = lds128(st + rowW1 + q);
         uint4 xv[NT];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) xv[j] = lds128(st + C::W_BYTES + uint32_t((8 * j + g) * kBK) + q);
+        for (int j = 0; j < NT; ++j) xv[j] = lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           uint32_t a0, a1, a2, a3;
@@ -354,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < NT; ++j) {
             uint32_t b0, b1;
             i8x4_to_f16(word_of(xv[j], ks), b0, b1);
-            mma_f16(accf[j], a0, a1, a2, a3, b0, b1);
+            mma_f16(accf[h % NACC][j], a0, a1, a2, a3, b0, b1);
           }
         }
       }
@@ -373,14 +391,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) {
-            acci[j][rr] += __float2int_rn(accf[j][rr]);
-            accf[j][rr] = 0.f;
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) {
+              acci[j][rr] += __float2int_rn(accf[a][j][rr]);
+              accf[a][j][rr] = 0.f;
+            }
           }
         nk = 0;
       }
       if (seg_end) {
         // ---- segment end: tile `tile`, k-blocks [seg_kb0, kb]
-        const TileCoord tc = decode_tile<MT, GROUPED>(p, tile, tile_start_s);
+        const TileCoord tc = decode_tile<MT, BN, GROUPED>(p, tile, tile_start_s);
         const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
         bool do_epi = whole;
         if (!whole) {
@@ -433,20 +454,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < NT; ++j)
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
-              const int nl = 16 * warp + g + ((rr & 2) ? 8 : 0);
-              const int ml = 8 * j + 2 * c + (rr & 1);
+              const int nl = 16 * warp + rg + ((rr & 2) ? 8 : 0);
+              const int ml = 8 * j + frag_row(2 * c + (rr & 1));
               const int n = tc.n0 + nl;
               float v = 0.f;
               if (ml < tc.rows && n < p.N)
                 v = __fmul_rn(__fmul_rn(__int2float_rn(acci[j][rr]), sxr[j][rr & 1]), swr[rr >> 1]);
-              epi[ml * kBN + nl] = f32_to_bf16_bits(v);
+              epi[ml * BN + nl] = f32_to_bf16_bits(v);
             }
           named_bar_sync(1, kCW * 32);
-          for (int idx = tid; idx < MT * (kBN / 8); idx += kCW * 32) {
-            const int ml = idx / (kBN / 8), c8 = idx % (kBN / 8);
+          for (int idx = tid; idx < MT * (BN / 8); idx += kCW * 32) {
+            const int ml = idx / (BN / 8), c8 = idx % (BN / 8);
             const int n = tc.n0 + c8 * 8;
             if (ml < tc.rows && n < p.N) {
-              const uint4 v = *reinterpret_cast<const uint4*>(epi + ml * kBN + c8 * 8);
+              const uint4 v = *reinterpret_cast<const uint4*>(epi + ml * BN + c8 * 8);
               *reinterpret_cast<uint4*>(p.y + int64_t(tc.x_row + ml) * p.N + n) = v;
             }
           }
@@ -499,19 +520,20 @@ size_t ws_w8a8_grouped_linear(int64_t R, int64_t K, int64_t N, int64_t E) {
   return kCounterBytes + slots_bytes(d.sm_count, 64);
 }
 
-template <int MT, bool GROUPED>
+template <int MT, int CW, bool GROUPED>
 static cudaError_t launch_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
                                cudaStream_t s, bool pdl) {
-  auto k = w8a8_gemm_kernel<MT, GROUPED>;
+  using C = Cfg<MT, CW>;
+  auto k = w8a8_gemm_kernel<MT, CW, GROUPED>;
   static uint64_t attr_done = 0;  // one bit per device id
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(attr_done & (1ull << (dev & 63)))) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << (dev & 63);
   }
-  return launch(k, dim3(grid), dim3(kThreads), size_t(Cfg<MT>::SMEM), s, pdl, *tw, *tx, p);
+  return launch(k, dim3(grid), dim3(C::THREADS), size_t(C::SMEM), s, pdl, *tw, *tx, p);
 }
 
 // Shared by the dense and fused entry points.  `counters` is the fixed
@@ -520,35 +542,48 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
                          int64_t N, uint16_t* y, uint32_t* counters, void* slots, size_t slots_avail, cudaStream_t s,
                          const DevInfo& d) {
   const int mt = pick_mt(M);
-  const int64_t m_tiles = (M + mt - 1) / mt, n_tiles = (N + kBN - 1) / kBN;
+  const int64_t m_tiles = (M + mt - 1) / mt;
+  const int KB = int((K + kBK - 1) / kBK);
+  // Schedule.  When tiles of 224 weight rows (14 consumer warps) give between
+  // 3/4 of and one tile per SM, every CTA streams one whole tile: no split-K,
+  // no partial sums.  Otherwise 128-row tiles are split stream-K over one CTA
+  // per SM.  (224-row tiles need MT <= 16 to fit the register file.)
+  const int64_t tiles224 = ((N + 223) / 224) * m_tiles;
+  const bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
+  const int64_t n_tiles = data_parallel ? (N + 223) / 224 : (N + kBN - 1) / kBN;
   const int64_t tiles = m_tiles * n_tiles;
-  if (tiles > kMaxTiles) return FQ_ERR_SHAPE;
-  if (slots_avail < slots_bytes(d.sm_count, mt)) return FQ_ERR_WORKSPACE;
+  if (tiles > kMaxTiles || int64_t(tiles) * KB > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
+  if (!data_parallel && slots_avail < slots_bytes(d.sm_count, mt)) return FQ_ERR_WORKSPACE;
   Problem p = {};
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
-  p.KB = int((K + kBK - 1) / kBK);
+  p.KB = KB;
   p.m_tiles = int(m_tiles);
   p.n_tiles = int(n_tiles);
-  p.total = tiles * p.KB;
+  p.total = tiles * KB;
   p.sx = sx;
   p.sw = sw;
   p.y = y;
   p.counters = counters;
   p.slots = static_cast<int32_t*>(slots);
   p.err = d.err_word;
-  const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, kBN);
+  const uint32_t bn = data_parallel ? 224u : uint32_t(kBN);
+  const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, bn);
   const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
   if (!tw || !tx) return FQ_ERR_CUDA;
-  const int grid = int(p.total < d.sm_count ? p.total : d.sm_count);
+  const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
   const bool pdl = pdl_enabled();
   cudaError_t e;
-  switch (mt) {
-    case 8: e = launch_gemm<8, false>(tw, tx, p, grid, s, pdl); break;
-    case 16: e = launch_gemm<16, false>(tw, tx, p, grid, s, pdl); break;
-    case 32: e = launch_gemm<32, false>(tw, tx, p, grid, s, pdl); break;
-    default: e = launch_gemm<64, false>(tw, tx, p, grid, s, pdl); break;
+  if (data_parallel) {
+    e = mt == 8 ? launch_gemm<8, 14, false>(tw, tx, p, grid, s, pdl) : launch_gemm<16, 14, false>(tw, tx, p, grid, s, pdl);
+  } else {
+    switch (mt) {
+      case 8: e = launch_gemm<8, 8, false>(tw, tx, p, grid, s, pdl); break;
+      case 16: e = launch_gemm<16, 8, false>(tw, tx, p, grid, s, pdl); break;
+      case 32: e = launch_gemm<32, 8, false>(tw, tx, p, grid, s, pdl); break;
+      default: e = launch_gemm<64, 8, false>(tw, tx, p, grid, s, pdl); break;
+    }
   }
   return cuda_status(e);
 }
@@ -654,7 +689,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(
   const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, uint32_t(mt));
   if (!tw || !tx) return FQ_ERR_CUDA;
   return cuda_status(
-      launch_gemm<mt, true>(tw, tx, p, d.sm_count, reinterpret_cast<cudaStream_t>(stream), pdl_enabled()));
+      launch_gemm<mt, 8, true>(tw, tx, p, d.sm_count, reinterpret_cast<cudaStream_t>(stream), pdl_enabled()));
 }
 
 // ================================================================ no-allocation variant
