@@ -27,18 +27,28 @@
 namespace fq {
 
 namespace es {
-constexpr int kBN = 128, kBK = 128, kCW = 8, kThreads = (kCW + 1) * 32;
+constexpr int kBK = 128;
+constexpr int kMaxGrid = 1024;
 
-template <int MT>
+// MT tokens per tile, CW consumer warps of 16 weight rows (BN = 16 * CW, a
+// divisor of the 128-wide weight-scale block), one producer warp.
+template <int MT, int CW>
 struct Cfg {
   static constexpr int NT = MT / 8;
-  static constexpr int W_BYTES = kBN * kBK;
+  static constexpr int BN = 16 * CW;
+  static constexpr int THREADS = (CW + 1) * 32;
+  static constexpr int W_BYTES = BN * kBK;
   static constexpr int X_BYTES = MT * kBK;
-  static constexpr int STAGE = W_BYTES + X_BYTES;
-  static constexpr int STAGES = MT <= 16 ? 8 : 6;
-  static constexpr int EPI = kBN * MT * 2;
-  static constexpr int SLOT = kBN * MT;  // fp32 per slot
-  static constexpr int SMEM = STAGES * STAGE + EPI + 2 * STAGES * 8 + 64 + 1024;
+  static constexpr int STAGE = W_BYTES + X_BYTES;  // multiple of 1024
+  static constexpr int EPI = BN * MT * 2;
+  static constexpr int SCALES = (MT + 4) * 4;      // per stage: MT token scale words + sw
+  // ~200 KB of weights in flight per SM to cover loaded HBM latency
+  static constexpr int STAGES_FIT = (212 * 1024 - EPI - 4096) / (STAGE + SCALES);
+  static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
+  static constexpr int SLOT = BN * MT;             // fp32 per slot
+  static constexpr int SMEM = STAGES * STAGE + EPI + STAGES * SCALES + 2 * STAGES * 8 + 64 + 1024;
+  static_assert(STAGES >= 3, "pipeline too shallow");
+  static_assert(128 % BN == 0, "tile must sit inside one weight-scale block");
 };
 
 struct Problem {
@@ -71,25 +81,32 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int s) {
   return s == 0 ? v.x : (s == 1 ? v.y : (s == 2 ? v.z : v.w));
 }
 
-// Activation scale of token t, group g, k-block kb (0 outside the tokens).
-__device__ __forceinline__ float load_sx(const Problem& p, int t, int g, int kb) {
-  if (t >= p.T) return 0.0f;
-  if (p.fmt == FQ_SCALE_UE8M0_PACKED) {
-    const int32_t* sp = static_cast<const int32_t*>(p.sx);
-    const uint32_t w = uint32_t(__ldg(sp + (int64_t(g) * p.P + (kb >> 2)) * p.Ta + t));
+// 4-byte asynchronous copy global -> shared (completion tracked by the
+// executing thread's cp.async group, announced on an mbarrier below).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (no pending-count increment: the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Decoded activation scale from its stored word: a packed UE8M0 word holds
+// four k-blocks' exponent bytes; an fp32 word is the scale itself.
+__device__ __forceinline__ float decode_sx(uint32_t w, int fmt, int kb) {
+  if (fmt == FQ_SCALE_UE8M0_PACKED) {
     const uint32_t u = (w >> (8 * (kb & 3))) & 0xFFu;
     return u ? __uint_as_float(u << 23) : __uint_as_float(0x00400000u);  // 2^(u-127)
   }
-  const float* sf = static_cast<const float*>(p.sx);
-  return __ldg(sf + (int64_t(t) * p.G + g) * p.KB + kb);
+  return __uint_as_float(w);
 }
-
-constexpr int kMaxGrid = 1024;
 
 // Fragment row g (0..7) of a 16-row block reads shared-memory row R(g), so the
 // two rows of each quarter-warp phase of a 16-byte ld.shared fall in different
 // halves of the 128-byte swizzle atom (conflict-free).
 __device__ __forceinline__ int frag_row(int g) { return (g >> 1) | ((g & 1) << 2); }
+
 // CTA whose stream-K range holds iteration i: the largest c with rb[c] <= i.
 __device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
   int lo = 0, hi = G;
@@ -100,7 +117,7 @@ __device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
   return lo;
 }
 
-// tile = (g * NB + nb) * TT + tt
+// tile = (g * NB + nb) * TT + tt, NB = N / BN
 struct ETile {
   int g, nb, tt;
 };
@@ -113,16 +130,17 @@ __device__ __forceinline__ ETile etile(const Problem& p, int tile) {
   return t;
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MT, int CW>
+__global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     fp8_einsum_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
-  using C = Cfg<MT>;
-  constexpr int NT = C::NT, S = C::STAGES;
+  using C = Cfg<MT, CW>;
+  constexpr int NT = C::NT, S = C::STAGES, BN = C::BN, kCW = CW, kThreads = C::THREADS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   uint16_t* epi = reinterpret_cast<uint16_t*>(smem + S * C::STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE + C::EPI);
+  uint32_t* scl = reinterpret_cast<uint32_t*>(smem + S * C::STAGE + C::EPI);  // [S][MT + 4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE + C::EPI + S * C::SCALES);
   uint64_t* empty = full + S;
   __shared__ int s_flag, s_issued, s_consumed;
   __shared__ volatile int s_abort;
@@ -131,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], 1 + 32);  // producer's expect-tx arrival + 32 scale-copy arrivals
       mbar_init(&empty[i], kCW);
     }
     fence_barrier_init();
@@ -148,18 +166,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int begin = rb[b], end = rb[b + 1];
   const int KB = p.KB;
+  const int NB128 = p.N / 128;
 
   if (warp == kCW) {
-    if (lane == 0 && end > begin) {
-      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+    // ------------------------------------------------ producer warp (all lanes)
+    if (end > begin) {
+      // weights streamed once (one token tile): evict-first; else keep for reuse
+      const uint64_t pol_w = p.TT > 1 ? policy_evict_normal() : policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
       const int n_it = end - begin;
       const int npre = n_it < S ? n_it : S;
-      {
+      if (lane == 0) {  // weights do not depend on the previous kernel: issue them first
         int tile = begin / KB, kb = begin - tile * KB;
         ETile t = etile(p, tile);
         for (int r = 0; r < npre; ++r) {
           mbar_arrive_expect_tx(&full[r], C::STAGE);
-          tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], kb * kBK, t.g * p.N + t.nb * kBN, pol_w);
+          tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], kb * kBK, t.g * p.N + t.nb * BN, pol_w);
           if (++kb == KB && r + 1 < npre) {
             kb = 0;
             t = etile(p, ++tile);
@@ -172,25 +194,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int r = 0; r < n_it; ++r) {
         const int s = r % S;
-        if (r < npre) {
-          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
-        } else {
-          if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
-            if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
-            s_abort = 1;
+        if (r >= npre) {
+          int ok = 1;
+          if (lane == 0) ok = (!s_abort && mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) ? 1 : 0;
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) {
+            if (lane == 0) {
+              if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+              s_abort = 1;
+            }
             break;
           }
-          mbar_arrive_expect_tx(&full[s], C::STAGE);
-          tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], kb * kBK, t.g * p.N + t.nb * kBN, pol_w);
-          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], C::STAGE);
+            tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], kb * kBK, t.g * p.N + t.nb * BN, pol_w);
+          }
         }
+        if (lane == 0)
+          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
+        // this stage's token scale words and the tile's weight-block scale
+        uint32_t* sc = scl + s * (MT + 4);
+        for (int m = lane; m < MT + 1; m += 32) {
+          const int tok = t.tt * MT + m;
+          if (m == MT) {
+            cp_async4(sc + MT, p.sw + (int64_t(t.g) * KB + kb) * NB128 + (t.nb * BN) / 128);
+          } else if (tok < p.T) {  // tokens past T are not copied; consumers use 0 for them
+            const void* src = (p.fmt == FQ_SCALE_UE8M0_PACKED)
+                                  ? static_cast<const void*>(static_cast<const int32_t*>(p.sx) +
+                                                             (int64_t(t.g) * p.P + (kb >> 2)) * p.Ta + tok)
+                                  : static_cast<const void*>(static_cast<const float*>(p.sx) +
+                                                             (int64_t(tok) * p.G + t.g) * KB + kb);
+            cp_async4(sc + m, src);
+          }
+        }
+        cp_async_arrive_noinc(&full[s]);
         ++issued;
         if (++kb == KB && r + 1 < n_it) {
           kb = 0;
           t = etile(p, ++tile);
         }
       }
-      s_issued = issued;
+      if (lane == 0) s_issued = issued;
     }
   } else {
     pdl_wait();
@@ -213,29 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool first_seg = true;
     int consumed = 0;
     const int n_it = end - begin;
-    // scales of the current k-block, fetched one iteration ahead
-    float sxv[NT][2], swv = 0.f;
-    auto fetch = [&](const ETile& et, int k, float out[NT][2], float& w) {
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) out[j][h] = load_sx(p, et.tt * MT + 8 * j + frag_row(2 * c + h), et.g, k);
-      w = __ldg(p.sw + (int64_t(et.g) * KB + k) * p.NB + et.nb);
-    };
-    if (n_it > 0) fetch(t, kb, sxv, swv);
-    // position of the next iteration (for the scale prefetch)
-    int ntile = tile, nkb = kb;
-    ETile nt_ = t;
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
-      float nsx[NT][2], nsw = 0.f;
-      if (r + 1 < n_it) {
-        if (++nkb == KB) {
-          nkb = 0;
-          nt_ = etile(p, ++ntile);
-        }
-        fetch(nt_, nkb, nsx, nsw);
-      }
       bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
@@ -266,12 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                        word_of(wb, 2 * ks + 1), word_of(xv, 2 * ks), word_of(xv, 2 * ks + 1));
           }
         }
-        if (NB2 == 2) {
+        const uint32_t* sc = scl + s * (MT + 4);
+        const float swv = __uint_as_float(sc[MT]);
+        float sxs[NT][2];
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
+        for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) blk[0][j][rr] = __fadd_rn(blk[0][j][rr], blk[NB2 - 1][j][rr]);
-        }
+          for (int hh = 0; hh < 2; ++hh) {
+            const int ml = 8 * j + frag_row(2 * c + hh);
+            sxs[j][hh] = (t.tt * MT + ml < p.T) ? decode_sx(sc[ml], p.fmt, kb) : 0.f;
+          }
         // The stage was read through the generic proxy (ld.shared); the next
         // TMA write into it goes through the async proxy.  Order the two
         // before handing the stage back, or TMA can overwrite it under the read.
@@ -282,14 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int rr = 0; rr < 4; ++rr) acc[j][rr] = __fmaf_rn(blk[0][j][rr], __fmul_rn(sxv[j][rr & 1], swv), acc[j][rr]);
+          for (int rr = 0; rr < 4; ++rr) {
+            const float bsum = NB2 == 2 ? __fadd_rn(blk[0][j][rr], blk[NB2 - 1][j][rr]) : blk[0][j][rr];
+            acc[j][rr] = __fmaf_rn(bsum, __fmul_rn(sxs[j][rr & 1], swv), acc[j][rr]);
+          }
       }
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        sxv[j][0] = nsx[j][0];
-        sxv[j][1] = nsx[j][1];
-      }
-      swv = nsw;
       if (kb == KB - 1 || r == n_it - 1) {
         const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
         bool do_epi = whole;
@@ -358,15 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int rr = 0; rr < 4; ++rr) {
               const int nl = 16 * warp + rg + ((rr & 2) ? 8 : 0);
               const int ml = 8 * j + frag_row(2 * c + (rr & 1));
-              epi[ml * kBN + nl] = f32_to_bf16_bits(acc[j][rr]);
+              epi[ml * BN + nl] = f32_to_bf16_bits(acc[j][rr]);
             }
           named_bar_sync(1, kCW * 32);
-          const int n0 = t.nb * kBN;
-          for (int idx = tid; idx < MT * (kBN / 8); idx += kCW * 32) {
-            const int ml = idx / (kBN / 8), c8 = idx % (kBN / 8);
+          const int n0 = t.nb * BN;
+          for (int idx = tid; idx < MT * (BN / 8); idx += kCW * 32) {
+            const int ml = idx / (BN / 8), c8 = idx % (BN / 8);
             const int tok = t.tt * MT + ml;
             if (tok < p.T) {
-              const uint4 v = *reinterpret_cast<const uint4*>(epi + ml * kBN + c8 * 8);
+              const uint4 v = *reinterpret_cast<const uint4*>(epi + ml * BN + c8 * 8);
               *reinterpret_cast<uint4*>(p.y + (int64_t(tok) * p.G + t.g) * p.N + n0 + c8 * 8) = v;
             }
           }
@@ -394,19 +418,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int pick_mt(int64_t T) { return T <= 8 ? 8 : (T <= 16 ? 16 : (T <= 32 ? 32 : 64)); }
 
-template <int MT>
+template <int MT, int CW>
 cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid, cudaStream_t s,
                       bool pdl) {
-  auto k = fp8_einsum_kernel<MT>;
+  using Cf = Cfg<MT, CW>;
+  auto k = fp8_einsum_kernel<MT, CW>;
   static uint64_t attr_done = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(attr_done & (1ull << (dev & 63)))) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << (dev & 63);
   }
-  return launch(k, dim3(grid), dim3(kThreads), size_t(Cfg<MT>::SMEM), s, pdl, *tw, *tx, p);
+  return launch(k, dim3(grid), dim3(Cf::THREADS), size_t(Cf::SMEM), s, pdl, *tw, *tx, p);
 }
 }  // namespace es
 
@@ -414,7 +439,7 @@ size_t ws_fp8_group_einsum(int64_t T, int64_t D, int64_t N, int64_t G) {
   DevInfo d;
   if (device_info(&d) != FQ_OK || T < 0 || D < 0 || N < 0 || G < 0) return 0;
   const int mt = es::pick_mt(T);
-  return kCounterBytes + size_t(2) * d.sm_count * es::kBN * mt * 4;
+  return kCounterBytes + size_t(2) * d.sm_count * 128 * mt * 4;
 }
 
 }  // namespace fq
@@ -438,20 +463,27 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(T) * G * N * 2, s));
   const int mt = es::pick_mt(T);
+  const int64_t TT = (T + mt - 1) / mt;
+  // Schedule: 64-row tiles, one whole tile per CTA, when they give between 3/4
+  // of and one tile per SM (no split-K); otherwise 128-row tiles split
+  // stream-K over one CTA per SM.
+  const int64_t tiles64 = G * (N / 64) * TT;
+  const bool data_parallel = tiles64 <= d.sm_count && tiles64 * 4 >= int64_t(d.sm_count) * 3;
+  const int bn = data_parallel ? 64 : 128;
   es::Problem p = {};
   p.T = int(T);
   p.G = int(G);
   p.D = int(D);
   p.N = int(N);
   p.KB = int(D / 128);
-  p.NB = int(N / 128);
-  p.TT = int((T + mt - 1) / mt);
+  p.NB = int(N / bn);
+  p.TT = int(TT);
   p.P = int((D / 128 + 3) / 4);
   p.Ta = int((T + 3) / 4 * 4);
-  const int64_t tiles = G * p.NB * int64_t(p.TT);
-  if (tiles > kMaxTiles) return FQ_ERR_SHAPE;
+  const int64_t tiles = G * p.NB * TT;
+  if (tiles > kMaxTiles || tiles * p.KB > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
   p.total = tiles * p.KB;
-  const size_t need = kCounterBytes + size_t(2) * d.sm_count * es::kBN * mt * 4;
+  const size_t need = kCounterBytes + size_t(2) * d.sm_count * 128 * mt * 4;
   if (!ws || ws_bytes < need) return FQ_ERR_WORKSPACE;
   if (!aligned16(ws)) return FQ_ERR_ALIGN;
   p.sx = sx;
@@ -461,17 +493,26 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   p.counters = static_cast<uint32_t*>(ws);
   p.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
   p.err = d.err_word;
-  const CUtensorMap* tw = tensor_map_u8_2d(w_gnd, uint64_t(D), uint64_t(G * N), uint64_t(D), es::kBK, es::kBN);
+  const CUtensorMap* tw = tensor_map_u8_2d(w_gnd, uint64_t(D), uint64_t(G * N), uint64_t(D), es::kBK, uint32_t(bn));
   const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(G * D), uint64_t(T), uint64_t(G * D), es::kBK, uint32_t(mt));
   if (!tw || !tx) return FQ_ERR_CUDA;
-  const int grid = int(p.total < d.sm_count ? p.total : d.sm_count);
+  const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
   const bool pdl = pdl_enabled();
   cudaError_t e;
-  switch (mt) {
-    case 8: e = es::launch_es<8>(tw, tx, p, grid, s, pdl); break;
-    case 16: e = es::launch_es<16>(tw, tx, p, grid, s, pdl); break;
-    case 32: e = es::launch_es<32>(tw, tx, p, grid, s, pdl); break;
-    default: e = es::launch_es<64>(tw, tx, p, grid, s, pdl); break;
+  if (data_parallel) {
+    switch (mt) {
+      case 8: e = es::launch_es<8, 4>(tw, tx, p, grid, s, pdl); break;
+      case 16: e = es::launch_es<16, 4>(tw, tx, p, grid, s, pdl); break;
+      case 32: e = es::launch_es<32, 4>(tw, tx, p, grid, s, pdl); break;
+      default: e = es::launch_es<64, 4>(tw, tx, p, grid, s, pdl); break;
+    }
+  } else {
+    switch (mt) {
+      case 8: e = es::launch_es<8, 8>(tw, tx, p, grid, s, pdl); break;
+      case 16: e = es::launch_es<16, 8>(tw, tx, p, grid, s, pdl); break;
+      case 32: e = es::launch_es<32, 8>(tw, tx, p, grid, s, pdl); break;
+      default: e = es::launch_es<64, 8>(tw, tx, p, grid, s, pdl); break;
+    }
   }
   return cuda_status(e);
 }

@@ -57,9 +57,11 @@ struct Cfg {
   static constexpr int X_BYTES = MT * kBK;
   static constexpr int STAGE = W_BYTES + X_BYTES;           // multiple of 1024
   static constexpr int EPI = BN * MT * 2;                   // bf16 staging
-  static constexpr int SMEM_BUDGET = 200 * 1024;
+  // Loaded HBM latency is several microseconds, so each SM needs ~200 KB of
+  // weights in flight to stream at full rate: fill the shared-memory budget.
+  static constexpr int SMEM_BUDGET = 212 * 1024;
   static constexpr int STAGES_FIT = (SMEM_BUDGET - EPI - 2048) / STAGE;
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
   static constexpr int SLOT = BN * MT;                      // int32 per slot
   static constexpr int SMEM = STAGES * STAGE + EPI + 2 * STAGES * 8 + 64 + 1024;  // + alignment slack
   static_assert(STAGES >= 3, "pipeline too shallow");
@@ -85,6 +87,7 @@ struct Problem {
   uint32_t* err;
   const int32_t* offsets;   // grouped: [E + 1]
   int E;                    // grouped: experts
+  int w_reuse;              // weight tiles are read by more than one token tile
 };
 
 // ---------------------------------------------------------------- device helpers
@@ -253,7 +256,10 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
   if (warp == kCW) {
     // ------------------------------------------------ producer warp
     if (lane == 0 && end > begin) {
-      const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+      // weights streamed once: evict-first; weights shared by several token
+      // tiles (large M, big experts) stay in L2 for the next token tile
+      const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
       const int n_it = end - begin;
       const int npre = n_it < S ? n_it : S;
       // weights do not depend on the previous kernel: issue them first
@@ -329,8 +335,10 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     // Dequant scales of the current tile, loaded when its segment starts so the
     // epilogue does not wait on a global round trip.
     float sxr[NT][2], swr[2];
+    int rows_cur = MT;  // valid activation rows of the current tile
     auto load_scales = [&](int t) {
       const TileCoord tc = decode_tile<MT, BN, GROUPED>(p, t, tile_start_s);
+      rows_cur = tc.rows;
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -360,6 +368,8 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
         const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
         const uint4 wa = lds128(st + rowW0 + q);
         const uint4 wb = lds128(st + rowW1 + q);
+        // 8-token groups past the tile's valid rows are skipped (uniform
+        // branch): an expert with 3 tokens in a 64-token tile costs one group
         uint4 xv[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) xv[j] = lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q);
@@ -370,9 +380,11 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
           i8x4_to_f16(word_of(wb, ks), a1, a3);
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            uint32_t b0, b1;
-            i8x4_to_f16(word_of(xv[j], ks), b0, b1);
-            mma_f16(accf[h % NACC][j], a0, a1, a2, a3, b0, b1);
+            if (8 * j < rows_cur) {
+              uint32_t b0, b1;
+              i8x4_to_f16(word_of(xv[j], ks), b0, b1);
+              mma_f16(accf[h % NACC][j], a0, a1, a2, a3, b0, b1);
+            }
           }
         }
       }
@@ -496,6 +508,228 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- cluster split-K
+//
+// For problems with too few weight tiles to fill the GPU (e.g. N = 1024), a
+// cluster of CL CTAs shares one tile of BN = 8 * CL weight rows and splits K.
+// Each CTA accumulates its K-range exactly (int32), then the partials are
+// reduce-scattered through distributed shared memory: CTA q of the cluster
+// owns rows [8q, 8q + 8) of the tile, receives the CL partial slices of those
+// rows, sums them, dequantizes and writes 16-byte rows of y.  No global
+// partial sums, counters or second pass.
+template <int MT, int CW, int CL>
+struct CCfg {
+  static constexpr int NT = MT / 8;
+  static constexpr int BN = 16 * CW;
+  static constexpr int THREADS = (CW + 1) * 32;
+  static constexpr int W_BYTES = BN * kBK;
+  static constexpr int X_BYTES = MT * kBK;
+  static constexpr int STAGE = W_BYTES + X_BYTES;
+  static constexpr int RECV = CL * 8 * MT * 4;  // [CL ranks][8 rows][MT tokens] int32
+  static constexpr int STAGES_FIT = (212 * 1024 - RECV - 2048) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
+  static constexpr int SMEM = STAGES * STAGE + RECV + 2 * STAGES * 8 + 64 + 1024;
+  static_assert(BN == 8 * CL, "each cluster rank owns 8 rows");
+  static_assert(STAGES >= 2, "pipeline too shallow");
+};
+
+template <int MT, int CW, int CL>
+__global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
+    w8a8_cluster_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
+  using C = CCfg<MT, CW, CL>;
+  constexpr int NT = C::NT, S = C::STAGES, BN = C::BN, kCW = CW;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  int32_t* recv = reinterpret_cast<int32_t*>(smem + S * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE + C::RECV);
+  uint64_t* empty = full + S;
+  __shared__ int s_issued, s_consumed;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = int(cluster_ctarank());
+  const int tile = blockIdx.x / CL;
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCW);
+    }
+    fence_barrier_init();
+    s_issued = 0;
+    s_consumed = 0;
+    s_abort = 0;
+  }
+  if (warp == kCW && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  // Every CTA of the cluster must be running before any distributed-smem
+  // write: arrive now, wait just before the scatter (keeps it off the
+  // critical path of the weight stream).
+  __syncwarp();
+  cluster_arrive_relaxed();
+
+  const int KB = p.KB;
+  const int kb0 = rank * KB / CL, kb1 = (rank + 1) * KB / CL;
+  const int n_it = kb1 - kb0;
+  const TileCoord tc = decode_tile<MT, BN, false>(p, tile, nullptr);
+  // epilogue scales of the rows this CTA owns (8 channels, one token per thread)
+  const int n_first = tc.n0 + 8 * rank;
+  float sw_own[8];
+  float sx_own = 0.f;
+#pragma unroll
+  for (int r2 = 0; r2 < 8; ++r2) sw_own[r2] = (n_first < p.N) ? __ldg(p.sw + tc.sw_base + n_first + r2) : 0.f;
+
+  if (warp == kCW) {
+    if (lane == 0 && n_it > 0) {
+      const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const int npre = n_it < S ? n_it : S;
+      for (int r = 0; r < npre; ++r) {
+        mbar_arrive_expect_tx(&full[r], C::STAGE);
+        tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], (kb0 + r) * kBK, tc.w_row, pol_w);
+      }
+      pdl_wait();
+      int issued = 0;
+      for (int r = 0; r < n_it; ++r) {
+        const int s = r % S;
+        if (r < npre) {
+          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], (kb0 + r) * kBK, tc.x_row, pol_x);
+        } else {
+          if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
+            if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+            s_abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], (kb0 + r) * kBK, tc.w_row, pol_w);
+          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], (kb0 + r) * kBK, tc.x_row, pol_x);
+        }
+        ++issued;
+      }
+      s_issued = issued;
+    }
+    __syncwarp();
+    cluster_wait_acquire();  // matches the consumers' wait before their scatter
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int g = lane >> 2, c = lane & 3;
+    const int rg = frag_row(g);
+    constexpr int NACC = NT <= 2 ? 2 : 1;
+    float accf[NACC][NT][4];
+    int acci[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+#pragma unroll
+        for (int a = 0; a < NACC; ++a) accf[a][j][r] = 0.f;
+        acci[j][r] = 0;
+      }
+    const uint32_t sbase = smem_u32(stages);
+    const uint32_t rowW0 = uint32_t((16 * warp + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
+    const int rows_cur = tc.rows;
+    int nk = 0, consumed = 0;
+    for (int r = 0; r < n_it; ++r) {
+      const int s = r % S;
+      bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
+      if (!ok) {
+        if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+        s_abort = 1;
+      }
+      const uint32_t st = sbase + uint32_t(s * C::STAGE);
+#pragma unroll
+      for (int h = 0; h < 2 && ok; ++h) {
+        const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
+        const uint4 wa = lds128(st + rowW0 + q);
+        const uint4 wb = lds128(st + rowW1 + q);
+        uint4 xv[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) xv[j] = lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          i8x4_to_f16(word_of(wa, ks), a0, a2);
+          i8x4_to_f16(word_of(wb, ks), a1, a3);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            if (8 * j < rows_cur) {
+              uint32_t b0, b1;
+              i8x4_to_f16(word_of(xv[j], ks), b0, b1);
+              mma_f16(accf[h % NACC][j], a0, a1, a2, a3, b0, b1);
+            }
+          }
+        }
+      }
+      // generic-proxy reads of the stage before the async-proxy refill
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (ok) {
+        if (lane == 0) mbar_arrive(&empty[s]);
+        ++consumed;
+      }
+      if (++nk == kFlushBlocks || r == n_it - 1) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) {
+              acci[j][rr] += __float2int_rn(accf[a][j][rr]);
+              accf[a][j][rr] = 0.f;
+            }
+        nk = 0;
+      }
+    }
+    if (tid < MT && tid < tc.rows) sx_own = __ldg(p.sx + tc.x_row + tid);
+    // reduce-scatter: row 16*warp + R(g) (+8) belongs to cluster rank 2*warp (+1)
+    cluster_wait_acquire();  // all CTAs of the cluster have started
+    const uint32_t recv_base = smem_u32(recv);
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int owner = 2 * warp + (rr >> 1);
+        const int ml = 8 * j + frag_row(2 * c + (rr & 1));
+        const uint32_t off = uint32_t(((rank * 8 + rg) * MT + ml) * 4);
+        st_cluster_u32(mapa_shared(recv_base + off, uint32_t(owner)), uint32_t(acci[j][rr]));
+      }
+    if (tid == 0) s_consumed = consumed;
+  }
+  // all partial slices have landed in their owners' shared memory
+  __syncwarp();
+  cluster_sync_all();
+  if (warp < kCW) {
+    // owner epilogue: rows [8 * rank, 8 * rank + 8) of the tile, one token per thread
+    for (int ml = tid; ml < MT; ml += kCW * 32) {  // MT <= 64 <= consumer threads: one pass
+      if (ml < tc.rows && n_first < p.N) {
+        const float sxv = sx_own;
+        uint32_t packed[4];
+#pragma unroll
+        for (int r2 = 0; r2 < 8; r2 += 2) {
+          int a0 = 0, a1 = 0;
+#pragma unroll
+          for (int rk = 0; rk < CL; ++rk) {
+            a0 += recv[(rk * 8 + r2) * MT + ml];
+            a1 += recv[(rk * 8 + r2 + 1) * MT + ml];
+          }
+          const float v0 = __fmul_rn(__fmul_rn(__int2float_rn(a0), sxv), sw_own[r2]);
+          const float v1 = __fmul_rn(__fmul_rn(__int2float_rn(a1), sxv), sw_own[r2 + 1]);
+          packed[r2 / 2] = uint32_t(f32_to_bf16_bits(v0)) | (uint32_t(f32_to_bf16_bits(v1)) << 16);
+        }
+        *reinterpret_cast<uint4*>(p.y + int64_t(tc.x_row + ml) * p.N + n_first) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int r = s_consumed; r < s_issued; ++r) mbar_wait(&full[r % S], uint32_t((r / S) & 1));
+  }
+}
+
 // ---------------------------------------------------------------- host side
 static int pick_mt(int64_t M) { return M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 32 ? 32 : 64)); }
 
@@ -536,6 +770,22 @@ static cudaError_t launch_gemm(const CUtensorMap* tw, const CUtensorMap* tx, con
   return launch(k, dim3(grid), dim3(C::THREADS), size_t(C::SMEM), s, pdl, *tw, *tx, p);
 }
 
+template <int MT>
+static cudaError_t launch_cluster_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
+                                       cudaStream_t s, bool pdl) {
+  using C = CCfg<MT, 2, 4>;
+  auto k = w8a8_cluster_kernel<MT, 2, 4>;
+  static uint64_t attr_done = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(attr_done & (1ull << (dev & 63)))) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done |= 1ull << (dev & 63);
+  }
+  return launch_cluster(k, dim3(grid), dim3(C::THREADS), size_t(C::SMEM), s, pdl, 4u, *tw, *tx, p);
+}
+
 // Shared by the dense and fused entry points.  `counters` is the fixed
 // counter block at the head of the workspace; `slots` the partial-sum area.
 fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K, const int8_t* w_nk, const float* sw,
@@ -550,6 +800,38 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   // per SM.  (224-row tiles need MT <= 16 to fit the register file.)
   const int64_t tiles224 = ((N + 223) / 224) * m_tiles;
   const bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
+  // Few tiles (small N): 32-row tiles, each split over K by a cluster of 4 CTAs
+  // with a distributed-shared-memory reduction, when that fills >= 1/2 the GPU.
+  const int64_t ctas_cl = ((N + 31) / 32) * m_tiles * 4;
+  const bool cluster = !data_parallel && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
+  if (cluster) {
+    Problem p = {};
+    p.M = int(M);
+    p.N = int(N);
+    p.K = int(K);
+    p.KB = KB;
+    p.m_tiles = int(m_tiles);
+    p.n_tiles = int((N + 31) / 32);
+    p.total = 0;
+    p.sx = sx;
+    p.sw = sw;
+    p.y = y;
+    p.err = d.err_word;
+    p.w_reuse = m_tiles > 1 ? 1 : 0;
+    const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, 32u);
+    const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
+    if (!tw || !tx) return FQ_ERR_CUDA;
+    const int grid = int(ctas_cl);
+    const bool pdl = pdl_enabled();
+    cudaError_t e;
+    switch (mt) {
+      case 8: e = launch_cluster_gemm<8>(tw, tx, p, grid, s, pdl); break;
+      case 16: e = launch_cluster_gemm<16>(tw, tx, p, grid, s, pdl); break;
+      case 32: e = launch_cluster_gemm<32>(tw, tx, p, grid, s, pdl); break;
+      default: e = launch_cluster_gemm<64>(tw, tx, p, grid, s, pdl); break;
+    }
+    return cuda_status(e);
+  }
   const int64_t n_tiles = data_parallel ? (N + 223) / 224 : (N + kBN - 1) / kBN;
   const int64_t tiles = m_tiles * n_tiles;
   if (tiles > kMaxTiles || int64_t(tiles) * KB > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
@@ -568,6 +850,7 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   p.counters = counters;
   p.slots = static_cast<int32_t*>(slots);
   p.err = d.err_word;
+  p.w_reuse = m_tiles > 1 ? 1 : 0;
   const uint32_t bn = data_parallel ? 224u : uint32_t(kBN);
   const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, bn);
   const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
@@ -685,6 +968,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(
   p.err = d.err_word;
   p.offsets = offsets;
   p.E = int(E);
+  p.w_reuse = 1;
   const CUtensorMap* tw = tensor_map_u8_2d(w_enk, uint64_t(K), uint64_t(E * N), uint64_t(K), kBK, kBN);
   const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, uint32_t(mt));
   if (!tw || !tx) return FQ_ERR_CUDA;
