@@ -587,6 +587,63 @@ def run_reference(args):
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(name):
+    """Run one op of the workload a few times, untimed, as a target for a profiler.
+
+    gemm_K1024_N32768 / gemm_K4096_N1024: the W8A8 GEMM once per M of the sweep,
+    each call on its own weight copy; einsum_T<T>: the block-scaled FP8 einsum
+    (G=8, D=4096, N=1024) three times; int8_quant_M16384: the per-token quant
+    at M=16384, K=4096 twice; fp8_group_quant_T4096: the group quant with packed
+    UE8M0 scales at T=4096, G=8, D=4096 twice.  Prints one status line."""
+    import torch
+    import fp8_dynamic_quant_gb300 as fq
+    from fp8_dynamic_quant_gb300 import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fq.lib()
+
+    def bf(a):
+        import numpy as np
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    launches = 0
+    if name.startswith("gemm_"):
+        K, N = {"gemm_K1024_N32768": (1024, 32768), "gemm_K4096_N1024": (4096, 1024)}[name]
+        ws = fq.new_workspace(fq.workspace_bytes(fq.OP_W8A8_LINEAR, 64, K, N), dev)
+        for i, M in enumerate(MS):
+            w = synth.uniform_int8_device((N, K), SEED + 100 * i + K + N, dev)
+            sw = synth.uniform_f32_device((N,), 1e-3, 1e-2, SEED + 7 + 100 * i + N, dev)
+            xq, sx = fq.dynamic_quant_int8(bf(synth.activations(M, K, SEED + 1000 + M + K)))
+            fq.w8a8_linear(xq, sx, w, sw, ws=ws)
+            launches += 1
+    elif name.startswith("einsum_T"):
+        T, G, D, N = int(name[len("einsum_T"):]), 8, 4096, 1024
+        w = torch.randn((G, N, D), generator=torch.Generator(device=dev).manual_seed(SEED + 50),
+                        device=dev, dtype=torch.float32) * 0.02
+        wq, sw = fq.quantize_weight_fp8_block(w)
+        del w
+        xq8, st = fq.quant_fp8_group_ue8m0_packed(bf(synth.group_activations(T, G, D, SEED + 3 + T)))
+        for _ in range(3):
+            fq.fp8_group_einsum(xq8, st, fq.SCALE_UE8M0_PACKED, wq, sw)
+            launches += 1
+    elif name == "int8_quant_M16384":
+        x = bf(synth.activations(16384, 4096, SEED + 9))
+        for _ in range(2):
+            fq.dynamic_quant_int8(x)
+            launches += 1
+    elif name == "fp8_group_quant_T4096":
+        x = bf(synth.group_activations(4096, 8, 4096, SEED + 2))
+        for _ in range(2):
+            fq.quant_fp8_group_ue8m0_packed(x)
+            launches += 1
+    else:
+        raise SystemExit("unknown profile case: " + name)
+    torch.cuda.synchronize()
+    st_, word = fq.device_error()
+    print(json.dumps({"profile_case": name, "op_calls": launches, "device_error": int(word)}))
+    return 0 if st_ == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -596,7 +653,11 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-call table, other configs and e2e")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--profile-case", default=None,
+                    help="run one op of the workload untimed (a profiler target) and exit; prints no bench line")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case)
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -14,7 +14,7 @@ __all__ = [
     "FqError", "lib", "lib_path", "dynamic_quant_int8", "w8a8_linear", "w8a8_quant_linear",
     "quant_fp8_group_ue8m0_packed", "quant_fp8_group_fp32", "pack_scales_ue8m0", "quantize_weight_fp8_block",
     "fp8_group_einsum", "scale_view", "moe_sort", "moe_gather_rows_i8", "w8a8_grouped_linear",
-    "swiglu_quant_int8", "moe_combine", "device_error", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
+    "swiglu_quant_int8", "moe_combine", "device_error", "selftest_wait_timeout", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
     "OP_W8A8_LINEAR", "OP_W8A8_QUANT_LINEAR", "OP_FP8_GROUP_EINSUM", "OP_MOE_SORT", "OP_W8A8_GROUPED_LINEAR",
 ]
 
@@ -31,6 +31,7 @@ _SIGS = {
     "fq_status_string": ([_I32], ctypes.c_char_p),
     "fq_last_cuda_error": ([], _I32),
     "fq_device_error": ([_P, _U32P], _I32),
+    "fq_selftest_wait_timeout": ([ctypes.c_uint64, _I32, _P], _I32),
     "fq_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64], _SZ),
     "dynamic_quant_int8": ([_P, _I64, _I64, _P, _P, _P], _I32),
     "w8a8_linear": ([_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P], _I32),
@@ -129,6 +130,13 @@ def device_error():
     w = ctypes.c_uint32(0)
     st = lib().fq_device_error(_stream(), ctypes.byref(w))
     return st, w.value
+
+
+def selftest_wait_timeout(budget_ns=1_000_000, arrive=False):
+    """Launch the bounded-wait self-test on the current stream (see fq.h);
+    with arrive=False the wait runs out and device_error() then reports
+    FQ_ERR_DEVICE_TIMEOUT."""
+    _check("fq_selftest_wait_timeout", lib().fq_selftest_wait_timeout(int(budget_ns), 1 if arrive else 0, _stream()))
 
 
 # ---------------------------------------------------------------- INT8 path

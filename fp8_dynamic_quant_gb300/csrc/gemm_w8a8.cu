@@ -36,6 +36,9 @@
 //    issued before griddepcontrol.wait, overlapping the previous kernel.
 #include <cuda_fp16.h>
 
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "fq_common.cuh"
@@ -786,6 +789,25 @@ static cudaError_t launch_cluster_gemm(const CUtensorMap* tw, const CUtensorMap*
   return launch_cluster(k, dim3(grid), dim3(C::THREADS), size_t(C::SMEM), s, pdl, 4u, *tw, *tx, p);
 }
 
+// Schedule override for tests and cliff studies: FQ_FORCE_SCHEDULE = dp |
+// cluster | streamk (read on every call).  A forced choice the shape cannot
+// take is ignored.  FQ_DEBUG_SCHEDULE=1 prints each decision to stderr.
+enum Sched { SCHED_AUTO = 0, SCHED_DP = 1, SCHED_CLUSTER = 2, SCHED_STREAMK = 3 };
+static int forced_schedule() {
+  const char* v = std::getenv("FQ_FORCE_SCHEDULE");
+  if (!v) return SCHED_AUTO;
+  if (!std::strcmp(v, "dp")) return SCHED_DP;
+  if (!std::strcmp(v, "cluster")) return SCHED_CLUSTER;
+  if (!std::strcmp(v, "streamk")) return SCHED_STREAMK;
+  return SCHED_AUTO;
+}
+static void debug_schedule(const char* op, int64_t M, int64_t K, int64_t N, int mt, const char* sched, int grid) {
+  const char* v = std::getenv("FQ_DEBUG_SCHEDULE");
+  if (v && v[0] == '1')
+    std::fprintf(stderr, "fq: %s M=%lld K=%lld N=%lld mt=%d schedule=%s grid=%d\n", op, (long long)M, (long long)K,
+                 (long long)N, mt, sched, grid);
+}
+
 // Shared by the dense and fused entry points.  `counters` is the fixed
 // counter block at the head of the workspace; `slots` the partial-sum area.
 fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K, const int8_t* w_nk, const float* sw,
@@ -799,11 +821,21 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   // no partial sums.  Otherwise 128-row tiles are split stream-K over one CTA
   // per SM.  (224-row tiles need MT <= 16 to fit the register file.)
   const int64_t tiles224 = ((N + 223) / 224) * m_tiles;
-  const bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
+  bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
   // Few tiles (small N): 32-row tiles, each split over K by a cluster of 4 CTAs
   // with a distributed-shared-memory reduction, when that fills >= 1/2 the GPU.
   const int64_t ctas_cl = ((N + 31) / 32) * m_tiles * 4;
-  const bool cluster = !data_parallel && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
+  bool cluster = !data_parallel && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
+  const int force = forced_schedule();
+  if (force == SCHED_DP && mt <= 16 && tiles224 <= kMaxGrid) {
+    data_parallel = true;
+    cluster = false;
+  } else if (force == SCHED_CLUSTER && KB >= 4 && ctas_cl <= (int64_t(1) << 30)) {
+    data_parallel = false;
+    cluster = true;
+  } else if (force == SCHED_STREAMK) {
+    data_parallel = cluster = false;
+  }
   if (cluster) {
     Problem p = {};
     p.M = int(M);
@@ -822,6 +854,7 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
     if (!tw || !tx) return FQ_ERR_CUDA;
     const int grid = int(ctas_cl);
+    debug_schedule("w8a8_linear", M, K, N, mt, "cluster4", grid);
     const bool pdl = pdl_enabled();
     cudaError_t e;
     switch (mt) {
@@ -856,6 +889,7 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
   if (!tw || !tx) return FQ_ERR_CUDA;
   const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
+  debug_schedule("w8a8_linear", M, K, N, mt, data_parallel ? "dp224" : "streamk", grid);
   const bool pdl = pdl_enabled();
   cudaError_t e;
   if (data_parallel) {

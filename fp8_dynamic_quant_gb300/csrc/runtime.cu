@@ -138,9 +138,37 @@ const CUtensorMap* tensor_map_u8_2d(const void* ptr, uint64_t cols, uint64_t row
   return &e.map;
 }
 
+// One warp: lane 0 waits on an mbarrier that only it can complete.  The
+// wait is the library's bounded wait; when it gives up, the timeout flag is
+// recorded exactly as the pipelined kernels record it.
+__global__ void selftest_wait_kernel(uint64_t budget_ns, int arrive) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    if (arrive) mbar_arrive(&bar);
+    if (!mbar_wait_ns(&bar, 0, budget_ns)) atomicOr(&g_error_word, DEVERR_TIMEOUT);
+  }
+  __syncwarp();
+}
+
 }  // namespace fq
 
 using namespace fq;
+
+extern "C" __attribute__((visibility("default"))) fq_status fq_selftest_wait_timeout(uint64_t budget_ns, int arrive,
+                                                                                     fq_stream_t stream) {
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  if (budget_ns < 1000ull) budget_ns = 1000ull;
+  if (budget_ns > 1000000000ull) budget_ns = 1000000000ull;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(budget_ns, arrive);
+  return cuda_status(cudaGetLastError());
+}
 
 extern "C" __attribute__((visibility("default"))) const char* fq_status_string(int s) {
   switch (s) {

@@ -83,6 +83,18 @@ int fq_last_cuda_error(void);
  * FQ_ERR_DEVICE_INPUT; *detail (nullable) receives the raw word. */
 fq_status fq_device_error(fq_stream_t stream, uint32_t* detail);
 
+/* Failure-detection self-test of the bounded device waits (no counterpart
+ * in the pages; it exercises the same wait loop every pipelined kernel uses).
+ * Launches one 32-thread block that initialises an mbarrier expecting one
+ * arrival and waits on it for at most `budget_ns` nanoseconds of
+ * %globaltimer time (clamped to [1000, 1e9]).  With arrive == 0 nothing ever
+ * arrives, the wait gives up, the kernel sets the timeout flag in the device
+ * error word and returns, so a following fq_device_error() reports
+ * FQ_ERR_DEVICE_TIMEOUT and the context stays usable.  With arrive != 0 the
+ * block arrives first and the wait completes (the control case).
+ * Returns FQ_OK once launched; asynchronous on `stream`. */
+fq_status fq_selftest_wait_timeout(uint64_t budget_ns, int arrive, fq_stream_t stream);
+
 /* Workspace sizing.  `op` is one of fq_op; the four sizes are read as:
  *   FQ_OP_W8A8_LINEAR, FQ_OP_W8A8_QUANT_LINEAR:   (M, K, N, unused)
  *   FQ_OP_FP8_GROUP_EINSUM:                       (T, D, N, G)

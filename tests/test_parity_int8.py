@@ -92,6 +92,18 @@ def test_w8a8_linear_bit_exact(M, K, N):
     assert np.array_equal(y, want), np.argwhere(y != want)[:5]
 
 
+@pytest.mark.parametrize("sched", ["dp", "cluster", "streamk"])
+@pytest.mark.parametrize("M,K,N", [(1, 1024, 4096), (8, 4096, 1024), (9, 2048, 2240), (16, 1024, 32768),
+                                   (3, 4112, 1040), (5, 512, 48)])
+def test_every_schedule_bit_exact(sched, M, K, N, monkeypatch):
+    # the host picks one of three schedules by shape; forcing each on the same
+    # problems checks that all three give the one correct answer
+    monkeypatch.setenv("FQ_FORCE_SCHEDULE", sched)
+    c = synth.int8_linear_case(M, K, N, 4000 + M + K + N)
+    q, s = oi8.dynamic_quant_int8(c["x"])
+    assert np.array_equal(gpu_linear(q, s, c["w_nk"], c["sw"]), oi8.w8a8_linear(q, s, c["w_nk"], c["sw"]))
+
+
 def test_w8a8_linear_accumulator_extremes():
     """|acc| up to 127*127*K with K = 131072 (the int32 limit) and mixed signs."""
     K, N = 131072, 32
