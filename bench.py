@@ -541,12 +541,12 @@ def cpu_baseline(budget_s=20.0):
         done_bytes += b
         n += 1
         i += 1
-        if time.perf_counter() - t0 >= budget_s or n >= len(calls):
+        if time.perf_counter() - t0 >= budget_s and n >= len(calls):
             break
     dt = time.perf_counter() - t0
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "%d of the %d oracle calls of one headline step (quant, GEMM, fused per linear and M), "
-                      "%.1f s of CPU time, numpy with the host BLAS threads" % (n, len(calls), dt)}
+            "sample": "%d oracle calls cycling over the %d calls of one headline step (quant, GEMM, fused per "
+                      "linear and M), %.1f s of CPU time, numpy with the host BLAS threads" % (n, len(calls), dt)}
 
 
 def run_reference(args):

@@ -733,16 +733,513 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- tcgen05 path (token tiles of 32 / 64)
+//
+// With 32 or more tokens per tile the mma.sync path above is bound by its own
+// instruction stream (the tensor pipe sits at a quarter of its time).  Here
+// the 5th-generation tensor cores take the MMA, with the weights as the A
+// operand in tensor memory and fp32 accumulators in tensor memory:
+//  - warp 0, lane 0: TMA producer of raw int8 stages (128 weight rows x 128 K
+//    and MT tokens x 128 K), the same stream-K walk as the kernel above;
+//  - warps 2..9: converters.  Warp w reaches tensor-memory lanes
+//    32*(w%4)..32*(w%4)+31 and takes K half (w-2)/4 of each k-block: every
+//    thread turns 64 bytes of its weight row into f16 pairs and stores them
+//    to the k-block's A stage with tcgen05.st.  Together they convert the
+//    activation tile into a 128-byte-swizzled K-major f16 operand in shared
+//    memory.
+//  - warp 1: allocates tensor memory; lane 0 issues tcgen05.mma kind::f16
+//    (M = 128 weight rows, N = MT tokens, K = 16) and commits each stage back.
+//  - warps 10..13: epilogue, one weight row per thread.  They drain each
+//    finished accumulator region into exact int32 sums kept in tensor memory
+//    and, at a segment's end, run the stream-K hand-off and the dequantizing
+//    store - while the converters and the tensor cores go on with the next
+//    segment.
+// Exactness: an int8 x int8 product is exact in fp32 and 1024 of them sum
+// below 2^24, so every 1024-K chunk accumulates in a fresh tensor-memory
+// region (two regions alternate) and is rounded to int32 (exact) on the way
+// out.
+namespace um {
+constexpr int kConvWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
+constexpr uint32_t kTmemCols = 512;
+
+// Tensor-memory columns: [2 buffers][CH chains] fp32 accumulator regions of
+// MT columns, then OP_STAGES A stages of 64 columns, then MT columns of
+// int32 segment sums.  At N = MT <= 64 one MMA is short next to its latency,
+// so the K steps of a chunk go round-robin to CH independent accumulators
+// that the tensor pipe can overlap.
+template <int MT>
+struct Cfg {
+  static constexpr int CH = MT == 32 ? 4 : 2;
+  static constexpr int ACC_COLS = 2 * CH * MT;
+  static constexpr int OP_FIT = (int(kTmemCols) - ACC_COLS - MT) / 64;
+  static constexpr int OP_STAGES = OP_FIT > 4 ? 4 : OP_FIT;
+  static constexpr int ISUM_COL = ACC_COLS + OP_STAGES * 64;
+  static constexpr int W_BYTES = 128 * kBK;       // raw weights of a stage
+  static constexpr int X_BYTES = MT * kBK;        // raw activations of a stage
+  static constexpr int RAW = W_BYTES + X_BYTES;   // multiple of 1024
+  static constexpr int XF = MT * kBK * 2;         // f16 activations: two 64-K halves of MT rows x 128 B
+  static constexpr int SMEM_BUDGET = 216 * 1024;
+  static constexpr int RAW_FIT = (SMEM_BUDGET - OP_STAGES * XF - 2048) / RAW;
+  static constexpr int RAW_STAGES = RAW_FIT > 12 ? 12 : RAW_FIT;
+  static constexpr int SLOT = 128 * MT;           // int32 per partial-sum slot
+  static constexpr int BAR_BYTES = (2 * RAW_STAGES + 2 * OP_STAGES + 4 + 1) * 8;
+  static constexpr int SMEM = RAW_STAGES * RAW + OP_STAGES * XF + BAR_BYTES + 1024;
+  static_assert(OP_STAGES >= 2, "operand pipeline too shallow");
+  static_assert(ISUM_COL + MT <= int(kTmemCols), "tensor-memory budget");
+  static_assert(RAW_STAGES >= 3, "pipeline too shallow");
+  static_assert(MT == 32 || MT == 64, "token tile");
+};
+}  // namespace um
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int MT, bool GROUPED>
+__global__ void __launch_bounds__(um::kThreads, 1)
+    w8a8_umma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
+  using C = um::Cfg<MT>;
+  constexpr int SR = C::RAW_STAGES, SO = C::OP_STAGES, XT = MT / 32, CH = C::CH;
+  constexpr int kThreads = um::kThreads, kConv = um::kConvWarps * 32, kEpi = um::kEpiWarps * 32;
+  constexpr int kEpiWarp0 = 2 + um::kConvWarps;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* raw = smem;
+  uint8_t* xf = smem + SR * C::RAW;
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(xf + SO * C::XF);
+  uint64_t* raw_empty = raw_full + SR;
+  uint64_t* op_full = raw_empty + SR;
+  uint64_t* op_empty = op_full + SO;
+  uint64_t* acc_full = op_empty + SO;   // [2]
+  uint64_t* acc_empty = acc_full + 2;   // [2]
+  uint64_t* done_bar = acc_empty + 2;
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(16) float s_sx[MT];
+  __shared__ __align__(16) uint16_t s_ystage[16 * 128];  // epilogue staging: 16 tokens x 128 rows of bf16
+  __shared__ int s_flag, s_issued, s_consumed;
+  __shared__ volatile int s_abort;  // set after any timed-out wait: later waits are skipped
+  __shared__ int tile_start_s[GROUPED ? 1025 : 1];
+  __shared__ int rb[kMaxGrid + 1];
+  __shared__ int wsum[kThreads / 32];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < SR; ++i) {
+      mbar_init(&raw_full[i], 1);
+      mbar_init(&raw_empty[i], um::kConvWarps);
+    }
+    for (int i = 0; i < SO; ++i) {
+      mbar_init(&op_full[i], um::kConvWarps);
+      mbar_init(&op_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], um::kEpiWarps);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+    s_issued = 0;
+    s_consumed = 0;
+    s_abort = 0;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, um::kTmemCols);
+    tmem_relinquish();
+  }
+
+  int64_t I = p.total;
+  if (GROUPED) {
+    // per-expert tile counts from the device offsets (written by moe_sort)
+    pdl_wait();
+    const int NB = p.n_tiles;
+    const int per = (p.E + kThreads - 1) / kThreads;
+    int local = 0;
+    for (int k = 0; k < per; ++k) {
+      const int e = tid * per + k;
+      if (e < p.E) {
+        const int me = p.offsets[e + 1] - p.offsets[e];
+        local += me > 0 ? NB * ((me + MT - 1) / MT) : 0;
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int k = 0; k < per; ++k) {
+      const int e = tid * per + k;
+      if (e < p.E) {
+        tile_start_s[e] = run;
+        const int me = p.offsets[e + 1] - p.offsets[e];
+        run += me > 0 ? NB * ((me + MT - 1) / MT) : 0;
+      }
+    }
+    if (tid == kThreads - 1) tile_start_s[p.E] = run;
+    __syncthreads();
+    I = int64_t(tile_start_s[p.E]) * p.KB;
+  }
+  const int G = gridDim.x, b = blockIdx.x;
+  for (int c = tid; c <= G; c += kThreads) rb[c] = int(int64_t(c) * I / G);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int begin = rb[b], end = rb[b + 1];
+  const int KB = p.KB;
+  const int n_it = end - begin;
+
+  if (warp == 0) {
+    // ------------------------------------------------ producer
+    if (lane == 0 && n_it > 0) {
+      const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      const int npre = n_it < SR ? n_it : SR;
+      {  // weights do not depend on the previous kernel: issue them first
+        int tile = begin / KB, kb = begin - tile * KB;
+        TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s);
+        for (int r = 0; r < npre; ++r) {
+          mbar_arrive_expect_tx(&raw_full[r], C::RAW);
+          tma_load_2d(raw + r * C::RAW, &tmW, &raw_full[r], kb * kBK, tc.w_row, pol_w);
+          if (++kb == KB && r + 1 < npre) {
+            kb = 0;
+            tc = decode_tile<MT, 128, GROUPED>(p, ++tile, tile_start_s);
+          }
+        }
+      }
+      pdl_wait();
+      int tile = begin / KB, kb = begin - tile * KB;
+      TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s);
+      int issued = 0;
+      for (int r = 0; r < n_it; ++r) {
+        const int s = r % SR;
+        if (r < npre) {
+          tma_load_2d(raw + s * C::RAW + C::W_BYTES, &tmX, &raw_full[s], kb * kBK, tc.x_row, pol_x);
+        } else {
+          if (s_abort || !mbar_wait(&raw_empty[s], uint32_t((r / SR - 1) & 1))) {
+            if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+            s_abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&raw_full[s], C::RAW);
+          tma_load_2d(raw + s * C::RAW, &tmW, &raw_full[s], kb * kBK, tc.w_row, pol_w);
+          tma_load_2d(raw + s * C::RAW + C::W_BYTES, &tmX, &raw_full[s], kb * kBK, tc.x_row, pol_x);
+        }
+        ++issued;
+        if (++kb == KB && r + 1 < n_it) {
+          kb = 0;
+          tc = decode_tile<MT, 128, GROUPED>(p, ++tile, tile_start_s);
+        }
+      }
+      s_issued = issued;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_f16_f32(128, MT);
+      const uint32_t xf_base = smem_u32(xf);
+      int kb = begin % KB, seg_kb0 = kb;
+      int ch = -1;  // accumulator chunk (1024 K of one segment); region ch & 1
+      for (int r = 0; r < n_it; ++r) {
+        const int so = r % SO;
+        const int kl = kb - seg_kb0;
+        const bool chunk_start = (kl % kFlushBlocks) == 0;
+        const bool seg_end = (kb == KB - 1) || (r == n_it - 1);
+        const bool chunk_end = seg_end || (kl % kFlushBlocks) == kFlushBlocks - 1;
+        if (chunk_start) ++ch;
+        bool ok = !s_abort;
+        if (ok && chunk_start && ch >= 2) ok = mbar_wait(&acc_empty[ch & 1], uint32_t(((ch >> 1) - 1) & 1));
+        if (ok) ok = mbar_wait(&op_full[so], uint32_t((r / SO) & 1));
+        if (!ok) {
+          if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+          s_abort = 1;
+        }
+        if (ok) {
+          tc_fence_after();
+          const uint32_t d = tmem + uint32_t((ch & 1) * CH * MT);
+          const uint32_t a = tmem + uint32_t(C::ACC_COLS + so * 64);
+          const uint32_t xs = xf_base + uint32_t(so * C::XF);
+#pragma unroll
+          for (int s = 0; s < 8; ++s)
+            umma_f16_ts(d + uint32_t((s % CH) * MT), a + uint32_t(8 * s),
+                        umma_desc_k_sw128(xs + uint32_t((s >> 2) * (MT * kBK) + (s & 3) * 32)), idesc,
+                        (!chunk_start || s >= CH) ? 1u : 0u);
+          umma_commit(&op_empty[so]);
+          if (chunk_end) umma_commit(&acc_full[ch & 1]);
+        }
+        if (seg_end) seg_kb0 = 0;
+        if (++kb == KB) kb = 0;
+      }
+      // every MMA issued above has finished once this arrives
+      umma_commit(done_bar);
+      if (!mbar_wait(done_bar, 0)) atomicOr(p.err, DEVERR_TIMEOUT);
+    }
+    __syncwarp();
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------ converters
+    pdl_wait();
+    // Let the next kernel launch only once this one's inputs are final: a
+    // dependent may prefetch weights before its own wait.
+    pdl_launch_dependents();
+    const int cw = warp - 2, q = warp & 3, hh = cw >> 2;
+    const int nl = 32 * q + lane;                       // weight row of the tile (tensor-memory lane)
+    const uint32_t lane_off = uint32_t(32 * q) << 16;
+    const uint32_t raw_base = smem_u32(raw), xf_base = smem_u32(xf);
+    int tile = begin / KB, kb = begin - tile * KB;
+    int consumed = 0;
+    int rows_cur = n_it > 0 ? decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s).rows : 0;
+    for (int r = 0; r < n_it; ++r) {
+      const int sr = r % SR, so = r % SO;
+      bool ok = !s_abort && mbar_wait(&raw_full[sr], uint32_t((r / SR) & 1));
+      if (ok && r >= SO) ok = mbar_wait(&op_empty[so], uint32_t((r / SO - 1) & 1));
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) {
+        if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      const uint32_t st = raw_base + uint32_t(sr * C::RAW);
+      uint4 v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = lds128(st + uint32_t(nl * kBK + (((4 * hh + c) ^ (nl & 7)) << 4)));
+      uint4 xv[XT];
+#pragma unroll
+      for (int t = 0; t < XT; ++t) {
+        const int task = t * kConv + cw * 32 + lane, xr = task >> 3, xc = task & 7;
+        if (xr < rows_cur) xv[t] = lds128(st + uint32_t(C::W_BYTES + xr * kBK + ((xc ^ (xr & 7)) << 4)));
+      }
+      uint32_t a[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) i8x4_to_f16(word_of(v[c], i), a[8 * c + 2 * i], a[8 * c + 2 * i + 1]);
+      tmem_st32(tmem + lane_off + uint32_t(C::ACC_COLS + so * 64 + 32 * hh), a);
+      const uint32_t xs = xf_base + uint32_t(so * C::XF);
+#pragma unroll
+      for (int t = 0; t < XT; ++t) {
+        const int task = t * kConv + cw * 32 + lane, xr = task >> 3, xc = task & 7;
+        if (xr < rows_cur) {
+          uint32_t f[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) i8x4_to_f16(word_of(xv[t], i), f[2 * i], f[2 * i + 1]);
+          const uint32_t rowb = xs + uint32_t((xc >> 2) * (MT * kBK) + xr * kBK);
+          const int j0 = 2 * (xc & 3);
+          sts128(rowb + uint32_t((j0 ^ (xr & 7)) << 4), f[0], f[1], f[2], f[3]);
+          sts128(rowb + uint32_t(((j0 + 1) ^ (xr & 7)) << 4), f[4], f[5], f[6], f[7]);
+        }
+      }
+      tmem_wait_st();
+      // the raw stage was read and the f16 operand written through the
+      // generic proxy; TMA (next raw fill) and the tensor cores read or write
+      // through the async proxy
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&raw_empty[sr]);
+        mbar_arrive(&op_full[so]);
+      }
+      ++consumed;
+      if (++kb == KB) {
+        kb = 0;
+        ++tile;
+        if (r + 1 < n_it) rows_cur = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s).rows;
+      }
+    }
+    if (tid == 64) s_consumed = consumed;
+  } else {
+    // ------------------------------------------------ epilogue
+    pdl_wait();
+    const int q = warp & 3;
+    const int nl = 32 * q + lane;                       // weight row of the tile (tensor-memory lane)
+    const int etid = tid - kEpiWarp0 * 32;
+    const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
+    const uint32_t tsum = trow + uint32_t(C::ISUM_COL);
+    int tile = begin / KB, kb = begin - tile * KB;
+    int seg_kb0 = kb;
+    bool first_seg = true;
+    int ch = -1;
+    for (int r = 0; r < n_it; ++r) {
+      const int kl = kb - seg_kb0;
+      const bool seg_end = (kb == KB - 1) || (r == n_it - 1);
+      const bool chunk_end = seg_end || (kl % kFlushBlocks) == kFlushBlocks - 1;
+      if ((kl % kFlushBlocks) == 0) ++ch;
+      if (chunk_end) {
+        // add region ch & 1, rounded to int32 (exact), into the segment's sums
+        // and hand the region back to the tensor cores
+        bool ok = !s_abort && mbar_wait(&acc_full[ch & 1], uint32_t((ch >> 1) & 1));
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+          if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+          s_abort = 1;
+        } else {
+          tc_fence_after();
+          const bool first_chunk = kl < kFlushBlocks;
+          // DW columns per round trip: every load of a piece is issued before one wait
+          constexpr int DW = (CH + 1) * 32 <= 96 ? 32 : 16;
+#pragma unroll
+          for (int h = 0; h < MT / DW; ++h) {
+            uint32_t sm[DW], f[CH][DW];
+            if constexpr (DW == 32) {
+              if (!first_chunk) tmem_ld32(tsum + uint32_t(DW * h), sm);
+#pragma unroll
+              for (int c = 0; c < CH; ++c) tmem_ld32(trow + uint32_t(((ch & 1) * CH + c) * MT + DW * h), f[c]);
+            } else {
+              if (!first_chunk) tmem_ld16(tsum + uint32_t(DW * h), sm);
+#pragma unroll
+              for (int c = 0; c < CH; ++c) tmem_ld16(trow + uint32_t(((ch & 1) * CH + c) * MT + DW * h), f[c]);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < DW; ++j) {
+              int32_t v = first_chunk ? 0 : int32_t(sm[j]);
+#pragma unroll
+              for (int c = 0; c < CH; ++c) v += __float2int_rn(__uint_as_float(f[c][j]));
+              sm[j] = uint32_t(v);
+            }
+            if constexpr (DW == 32) tmem_st32(tsum + uint32_t(DW * h), sm); else tmem_st16(tsum + uint32_t(DW * h), sm);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ch & 1]);
+        }
+      }
+      if (seg_end) {
+        // ---- segment end: tile `tile`, k-blocks [seg_kb0, kb]
+        const TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s);
+        const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
+        bool do_epi = whole;
+        if (!whole) {
+          int32_t* my = p.slots + (2 * b + (first_seg ? 0 : 1)) * int64_t(C::SLOT) + nl;
+#pragma unroll
+          for (int h = 0; h < MT / 16; ++h) {
+            uint32_t sm[16];
+            tmem_ld16(tsum + uint32_t(16 * h), sm);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) my[(16 * h + j) * 128] = int32_t(sm[j]);
+          }
+          named_bar_sync(1, kEpi);
+          if (etid == 0) {
+            const uint32_t nb = uint32_t(kb - seg_kb0 + 1);
+            const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile], nb);
+            const int last = (old + nb == uint32_t(KB)) ? 1 : 0;
+            if (last) p.counters[tile] = 0;  // every contributor has arrived; ready for the next call
+            s_flag = last;
+          }
+          named_bar_sync(1, kEpi);
+          do_epi = s_flag != 0;
+        }
+        if (do_epi) {
+          // do_epi is uniform over the epilogue warps (whole, or s_flag)
+          if (etid < MT) s_sx[etid] = etid < tc.rows ? __ldg(p.sx + tc.x_row + etid) : 0.f;
+          named_bar_sync(1, kEpi);
+          const int c0 = whole ? 0 : cta_of(rb, G, tile * KB), c1 = whole ? -1 : cta_of(rb, G, tile * KB + KB - 1);
+          const int n = tc.n0 + nl;
+          const float swv = n < p.N ? __ldg(p.sw + tc.sw_base + n) : 0.f;  // rows past N are never stored
+          // add the other contributors' partial sums into the tensor-memory
+          // sums: all MT values of a contributor are loaded in one batch
+          for (int cc = c0; cc <= c1; ++cc) {
+            // skip self and CTAs with an empty range (more CTAs than iterations)
+            if (cc == b || rb[cc + 1] == rb[cc]) continue;
+            const int first_tile = rb[cc] / KB;
+            const int32_t* sl = p.slots + (2 * int64_t(cc) + (first_tile == tile ? 0 : 1)) * int64_t(C::SLOT) + nl;
+            int32_t v[MT];
+#pragma unroll
+            for (int j = 0; j < MT; ++j) v[j] = __ldcg(sl + j * 128);
+#pragma unroll
+            for (int h = 0; h < MT / 16; ++h) {
+              uint32_t sm[16];
+              tmem_ld16(tsum + uint32_t(16 * h), sm);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sm[j] = uint32_t(int32_t(sm[j]) + v[16 * h + j]);
+              tmem_st16(tsum + uint32_t(16 * h), sm);
+            }
+            tmem_wait_st();
+          }
+#pragma unroll
+          for (int h = 0; h < MT / 16; ++h) {
+            uint32_t sm[16];
+            tmem_ld16(tsum + uint32_t(16 * h), sm);
+            tmem_wait_ld();
+            int32_t acc[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[j] = int32_t(sm[j]);
+            // dequantize 16 tokens of this row into the staging tile
+            // [16 tokens][128 rows], then write whole 16-byte pieces of y rows
+            float sxv[16];
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const float4 t = *reinterpret_cast<const float4*>(&s_sx[16 * h + j]);
+              sxv[j] = t.x;
+              sxv[j + 1] = t.y;
+              sxv[j + 2] = t.z;
+              sxv[j + 3] = t.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              s_ystage[j * 128 + nl] = f32_to_bf16_bits(__fmul_rn(__fmul_rn(__int2float_rn(acc[j]), sxv[j]), swv));
+            named_bar_sync(1, kEpi);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int piece = i * kEpi + etid, j = piece >> 4, c8 = piece & 15;  // 16 pieces of 8 per token
+              const int m = 16 * h + j, nn = tc.n0 + 8 * c8;
+              if (m < tc.rows && nn < p.N) {
+                const uint4 v = *reinterpret_cast<const uint4*>(&s_ystage[j * 128 + 8 * c8]);
+                st_global_v4(p.y + int64_t(tc.x_row + m) * p.N + nn, v);
+              }
+            }
+            named_bar_sync(1, kEpi);
+          }
+          named_bar_sync(1, kEpi);  // s_sx is rewritten by the next segment
+        }
+        tc_fence_before();
+        first_seg = false;
+        seg_kb0 = 0;
+      }
+      if (++kb == KB) {
+        kb = 0;
+        ++tile;
+      }
+    }
+  }
+  __syncthreads();
+  // Drain: on the normal path every issued stage was consumed.  After a
+  // timeout, wait (bounded) for copies still in flight before exiting.
+  if (tid == 0) {
+    for (int r = s_consumed; r < s_issued; ++r) mbar_wait(&raw_full[r % SR], uint32_t((r / SR) & 1));
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, um::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 static int pick_mt(int64_t M) { return M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 32 ? 32 : 64)); }
 
 static size_t slots_bytes(int sms, int mt) { return size_t(2) * sms * kBN * mt * 4; }
+// Token tile the partial-sum slots are sized for: the tcgen05 kernel runs
+// tiles of at least 32 tokens (a forced schedule may run it for any M).
+static int slots_mt(int64_t M) { return pick_mt(M) < 32 ? 32 : pick_mt(M); }
 
 // Workspace layout: [counters: kCounterBytes][xq, sx: fused call only][partial-sum slots]
 size_t ws_w8a8_linear(int64_t M, int64_t K, int64_t N) {
   DevInfo d;
   if (device_info(&d) != FQ_OK || M < 0 || K < 0 || N < 0) return 0;
-  return kCounterBytes + slots_bytes(d.sm_count, pick_mt(M));
+  return kCounterBytes + slots_bytes(d.sm_count, slots_mt(M));
 }
 
 size_t ws_w8a8_quant_linear(int64_t M, int64_t K, int64_t N) {
@@ -773,6 +1270,22 @@ static cudaError_t launch_gemm(const CUtensorMap* tw, const CUtensorMap* tx, con
   return launch(k, dim3(grid), dim3(C::THREADS), size_t(C::SMEM), s, pdl, *tw, *tx, p);
 }
 
+template <int MT, bool GROUPED>
+static cudaError_t launch_umma_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
+                                    cudaStream_t s, bool pdl) {
+  using C = um::Cfg<MT>;
+  auto k = w8a8_umma_kernel<MT, GROUPED>;
+  static uint64_t attr_done = 0;  // one bit per device id
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(attr_done & (1ull << (dev & 63)))) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_done |= 1ull << (dev & 63);
+  }
+  return launch(k, dim3(grid), dim3(um::kThreads), size_t(C::SMEM), s, pdl, *tw, *tx, p);
+}
+
 template <int MT>
 static cudaError_t launch_cluster_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
                                        cudaStream_t s, bool pdl) {
@@ -790,15 +1303,16 @@ static cudaError_t launch_cluster_gemm(const CUtensorMap* tw, const CUtensorMap*
 }
 
 // Schedule override for tests and cliff studies: FQ_FORCE_SCHEDULE = dp |
-// cluster | streamk (read on every call).  A forced choice the shape cannot
-// take is ignored.  FQ_DEBUG_SCHEDULE=1 prints each decision to stderr.
-enum Sched { SCHED_AUTO = 0, SCHED_DP = 1, SCHED_CLUSTER = 2, SCHED_STREAMK = 3 };
+// cluster | streamk | umma (read on every call).  A forced choice the shape
+// cannot take is ignored.  FQ_DEBUG_SCHEDULE=1 prints each decision to stderr.
+enum Sched { SCHED_AUTO = 0, SCHED_DP = 1, SCHED_CLUSTER = 2, SCHED_STREAMK = 3, SCHED_UMMA = 4 };
 static int forced_schedule() {
   const char* v = std::getenv("FQ_FORCE_SCHEDULE");
   if (!v) return SCHED_AUTO;
   if (!std::strcmp(v, "dp")) return SCHED_DP;
   if (!std::strcmp(v, "cluster")) return SCHED_CLUSTER;
   if (!std::strcmp(v, "streamk")) return SCHED_STREAMK;
+  if (!std::strcmp(v, "umma")) return SCHED_UMMA;
   return SCHED_AUTO;
 }
 static void debug_schedule(const char* op, int64_t M, int64_t K, int64_t N, int mt, const char* sched, int grid) {
@@ -833,9 +1347,14 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   } else if (force == SCHED_CLUSTER && KB >= 4 && ctas_cl <= (int64_t(1) << 30)) {
     data_parallel = false;
     cluster = true;
-  } else if (force == SCHED_STREAMK) {
+  } else if (force == SCHED_STREAMK || force == SCHED_UMMA) {
     data_parallel = cluster = false;
   }
+  // Stream-K with token tiles of 32 or 64 runs on the tcgen05 kernel (the
+  // mma.sync kernel is instruction-bound there).
+  const bool umma = !data_parallel && !cluster &&
+                    (force == SCHED_UMMA ? true : (force == SCHED_STREAMK ? false : mt >= 32));
+  const int mt_run = umma && mt < 32 ? 32 : mt;
   if (cluster) {
     Problem p = {};
     p.M = int(M);
@@ -866,15 +1385,16 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     return cuda_status(e);
   }
   const int64_t n_tiles = data_parallel ? (N + 223) / 224 : (N + kBN - 1) / kBN;
-  const int64_t tiles = m_tiles * n_tiles;
+  const int64_t m_tiles_run = (M + mt_run - 1) / mt_run;
+  const int64_t tiles = m_tiles_run * n_tiles;
   if (tiles > kMaxTiles || int64_t(tiles) * KB > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
-  if (!data_parallel && slots_avail < slots_bytes(d.sm_count, mt)) return FQ_ERR_WORKSPACE;
+  if (!data_parallel && slots_avail < slots_bytes(d.sm_count, mt_run)) return FQ_ERR_WORKSPACE;
   Problem p = {};
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
   p.KB = KB;
-  p.m_tiles = int(m_tiles);
+  p.m_tiles = int(m_tiles_run);
   p.n_tiles = int(n_tiles);
   p.total = tiles * KB;
   p.sx = sx;
@@ -883,16 +1403,19 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   p.counters = counters;
   p.slots = static_cast<int32_t*>(slots);
   p.err = d.err_word;
-  p.w_reuse = m_tiles > 1 ? 1 : 0;
+  p.w_reuse = m_tiles_run > 1 ? 1 : 0;
   const uint32_t bn = data_parallel ? 224u : uint32_t(kBN);
   const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, bn);
-  const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
+  const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt_run));
   if (!tw || !tx) return FQ_ERR_CUDA;
   const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
-  debug_schedule("w8a8_linear", M, K, N, mt, data_parallel ? "dp224" : "streamk", grid);
+  debug_schedule("w8a8_linear", M, K, N, mt_run, data_parallel ? "dp224" : (umma ? "umma" : "streamk"), grid);
   const bool pdl = pdl_enabled();
   cudaError_t e;
-  if (data_parallel) {
+  if (umma) {
+    e = mt_run == 32 ? launch_umma_gemm<32, false>(tw, tx, p, grid, s, pdl)
+                     : launch_umma_gemm<64, false>(tw, tx, p, grid, s, pdl);
+  } else if (data_parallel) {
     e = mt == 8 ? launch_gemm<8, 14, false>(tw, tx, p, grid, s, pdl) : launch_gemm<16, 14, false>(tw, tx, p, grid, s, pdl);
   } else {
     switch (mt) {
@@ -956,7 +1479,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
   float* sx = sx_out ? sx_out : reinterpret_cast<float*>(w8 + kCounterBytes + xq_b);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // validate the GEMM part before launching the quant
-  if (N > 0 && K > 0 && ws_bytes - kCounterBytes - xq_b - sx_b < slots_bytes(d.sm_count, pick_mt(M)))
+  if (N > 0 && K > 0 && ws_bytes - kCounterBytes - xq_b - sx_b < slots_bytes(d.sm_count, slots_mt(M)))
     return FQ_ERR_WORKSPACE;
   if ((st = dynamic_quant_int8(x, M, K, xq, sx, stream)) != FQ_OK) return st;
   if (N == 0) return FQ_OK;
@@ -1006,8 +1529,11 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(
   const CUtensorMap* tw = tensor_map_u8_2d(w_enk, uint64_t(K), uint64_t(E * N), uint64_t(K), kBK, kBN);
   const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, uint32_t(mt));
   if (!tw || !tx) return FQ_ERR_CUDA;
-  return cuda_status(
-      launch_gemm<mt, 8, true>(tw, tx, p, d.sm_count, reinterpret_cast<cudaStream_t>(stream), pdl_enabled()));
+  const bool umma = forced_schedule() != SCHED_STREAMK;
+  debug_schedule("w8a8_grouped_linear", R, K, N, mt, umma ? "umma" : "streamk", d.sm_count);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(umma ? launch_umma_gemm<mt, true>(tw, tx, p, d.sm_count, s, pdl_enabled())
+                          : launch_gemm<mt, 8, true>(tw, tx, p, d.sm_count, s, pdl_enabled()));
 }
 
 // ================================================================ no-allocation variant

@@ -92,9 +92,10 @@ def test_w8a8_linear_bit_exact(M, K, N):
     assert np.array_equal(y, want), np.argwhere(y != want)[:5]
 
 
-@pytest.mark.parametrize("sched", ["dp", "cluster", "streamk"])
+@pytest.mark.parametrize("sched", ["dp", "cluster", "streamk", "umma"])
 @pytest.mark.parametrize("M,K,N", [(1, 1024, 4096), (8, 4096, 1024), (9, 2048, 2240), (16, 1024, 32768),
-                                   (3, 4112, 1040), (5, 512, 48)])
+                                   (3, 4112, 1040), (5, 512, 48), (32, 4096, 1024), (64, 1024, 32768),
+                                   (50, 3968, 2064), (64, 16, 128), (40, 1024, 128)])
 def test_every_schedule_bit_exact(sched, M, K, N, monkeypatch):
     # the host picks one of three schedules by shape; forcing each on the same
     # problems checks that all three give the one correct answer

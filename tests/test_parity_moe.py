@@ -49,8 +49,13 @@ def test_gather_exact():
     assert np.array_equal(sg.cpu().numpy(), omoe.gather_rows(os_, operm, topk))
 
 
-@pytest.mark.parametrize("R,E,K,N", [(64, 8, 256, 256), (300, 16, 1024, 384), (5, 3, 128, 128), (2048, 64, 512, 256)])
-def test_grouped_linear_exact(R, E, K, N):
+@pytest.mark.parametrize("sched", ["auto", "streamk"])
+@pytest.mark.parametrize("R,E,K,N", [(64, 8, 256, 256), (300, 16, 1024, 384), (5, 3, 128, 128), (2048, 64, 512, 256),
+                                     (700, 12, 4096, 256), (90, 5, 4224, 128)])
+def test_grouped_linear_exact(R, E, K, N, sched, monkeypatch):
+    # auto runs the tcgen05 kernel for K <= 4096; streamk forces the mma.sync kernel
+    if sched != "auto":
+        monkeypatch.setenv("FQ_FORCE_SCHEDULE", sched)
     r = np.random.default_rng(R + E)
     counts = r.multinomial(R, r.dirichlet(np.ones(E) * 0.3))
     counts[0] = 0 if E > 2 else counts[0]                     # an empty expert
