@@ -22,6 +22,9 @@
 //    and fp32-scale calls produce identical bits.
 //  * The scale format only changes how sx is decoded: packed byte
 //    ((g*P + kb/4)*Ta + t)*4 + kb%4 -> 2^(u-127), or the fp32 value.
+#include <cstdlib>
+#include <cstring>
+
 #include "fq_common.cuh"
 
 namespace fq {
@@ -85,6 +88,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int s) {
 // executing thread's cp.async group, announced on an mbarrier below).
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (no pending-count increment: the barrier's count includes this arrival).
@@ -214,17 +220,21 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
           tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
         // this stage's token scale words and the tile's weight-block scale
         uint32_t* sc = scl + s * (MT + 4);
-        for (int m = lane; m < MT + 1; m += 32) {
-          const int tok = t.tt * MT + m;
-          if (m == MT) {
-            cp_async4(sc + MT, p.sw + (int64_t(t.g) * KB + kb) * NB128 + (t.nb * BN) / 128);
-          } else if (tok < p.T) {  // tokens past T are not copied; consumers use 0 for them
-            const void* src = (p.fmt == FQ_SCALE_UE8M0_PACKED)
-                                  ? static_cast<const void*>(static_cast<const int32_t*>(p.sx) +
-                                                             (int64_t(t.g) * p.P + (kb >> 2)) * p.Ta + tok)
-                                  : static_cast<const void*>(static_cast<const float*>(p.sx) +
-                                                             (int64_t(tok) * p.G + t.g) * KB + kb);
-            cp_async4(sc + m, src);
+        if (lane == 0) cp_async4(sc + MT, p.sw + (int64_t(t.g) * KB + kb) * NB128 + (t.nb * BN) / 128);
+        if (p.fmt == FQ_SCALE_UE8M0_PACKED) {
+          // packed words of 4 consecutive tokens are contiguous and 16-byte
+          // aligned (the token dimension is padded to a multiple of 4)
+          for (int c4 = lane; c4 < MT / 4; c4 += 32) {
+            const int tok0 = t.tt * MT + 4 * c4;
+            if (tok0 < p.Ta)
+              cp_async16(sc + 4 * c4,
+                         static_cast<const int32_t*>(p.sx) + (int64_t(t.g) * p.P + (kb >> 2)) * p.Ta + tok0);
+          }
+        } else {
+          for (int m = lane; m < MT; m += 32) {
+            const int tok = t.tt * MT + m;
+            if (tok < p.T)  // tokens past T are not copied; consumers use 0 for them
+              cp_async4(sc + m, static_cast<const float*>(p.sx) + (int64_t(tok) * p.G + t.g) * KB + kb);
           }
         }
         cp_async_arrive_noinc(&full[s]);
@@ -464,11 +474,16 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   if (D == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(T) * G * N * 2, s));
   const int mt = es::pick_mt(T);
   const int64_t TT = (T + mt - 1) / mt;
-  // Schedule: 64-row tiles, one whole tile per CTA, when they give between 3/4
-  // of and one tile per SM (no split-K); otherwise 128-row tiles split
-  // stream-K over one CTA per SM.
+  // Schedule: 128-row tiles split stream-K over one CTA per SM.  The other
+  // schedule - 64-row tiles, one whole tile per CTA - measured slower on GB300
+  // at every decode size (T = 1..256) and is only taken when forced.
   const int64_t tiles64 = G * (N / 64) * TT;
-  const bool data_parallel = tiles64 <= d.sm_count && tiles64 * 4 >= int64_t(d.sm_count) * 3;
+  bool data_parallel = false;
+  // FQ_FORCE_SCHEDULE = dp | streamk overrides the choice (tests and studies)
+  if (const char* f = std::getenv("FQ_FORCE_SCHEDULE")) {
+    if (!std::strcmp(f, "dp") && tiles64 <= es::kMaxGrid) data_parallel = true;
+    if (!std::strcmp(f, "streamk")) data_parallel = false;
+  }
   const int bn = data_parallel ? 64 : 128;
   es::Problem p = {};
   p.T = int(T);
@@ -493,9 +508,12 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   p.counters = static_cast<uint32_t*>(ws);
   p.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
   p.err = d.err_word;
-  const CUtensorMap* tw = tensor_map_u8_2d(w_gnd, uint64_t(D), uint64_t(G * N), uint64_t(D), es::kBK, uint32_t(bn));
-  const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(G * D), uint64_t(T), uint64_t(G * D), es::kBK, uint32_t(mt));
-  if (!tw || !tx) return FQ_ERR_CUDA;
+  CUtensorMap tw_map, tx_map;
+  if (!tensor_map_u8_2d(&tw_map, w_gnd, uint64_t(D), uint64_t(G * N), uint64_t(D), es::kBK, uint32_t(bn)) ||
+      !tensor_map_u8_2d(&tx_map, xq, uint64_t(G * D), uint64_t(T), uint64_t(G * D), es::kBK, uint32_t(mt)))
+    return FQ_ERR_CUDA;
+  const CUtensorMap* tw = &tw_map;
+  const CUtensorMap* tx = &tx_map;
   const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
   const bool pdl = pdl_enabled();
   cudaError_t e;

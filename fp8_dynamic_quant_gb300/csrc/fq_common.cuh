@@ -291,9 +291,10 @@ fq_status cuda_status(cudaError_t e);
 
 // Encodes a 2-D 8-bit tensor map (inner dimension `cols` bytes, `rows` rows,
 // row pitch `pitch` bytes) with a box of box_cols x box_rows and 128-byte
-// swizzle; cached per thread by (ptr, sizes).  Returns nullptr on failure.
-const CUtensorMap* tensor_map_u8_2d(const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
-                                    uint32_t box_cols, uint32_t box_rows);
+// swizzle, written to *out; encodings are cached per thread by (ptr, sizes).
+// Returns false on failure.
+bool tensor_map_u8_2d(CUtensorMap* out, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
+                      uint32_t box_cols, uint32_t box_rows);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

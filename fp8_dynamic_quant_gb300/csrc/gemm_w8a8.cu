@@ -1369,9 +1369,12 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     p.y = y;
     p.err = d.err_word;
     p.w_reuse = m_tiles > 1 ? 1 : 0;
-    const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, 32u);
-    const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt));
-    if (!tw || !tx) return FQ_ERR_CUDA;
+    CUtensorMap tw_map, tx_map;
+    if (!tensor_map_u8_2d(&tw_map, w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, 32u) ||
+        !tensor_map_u8_2d(&tx_map, xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt)))
+      return FQ_ERR_CUDA;
+    const CUtensorMap* tw = &tw_map;
+    const CUtensorMap* tx = &tx_map;
     const int grid = int(ctas_cl);
     debug_schedule("w8a8_linear", M, K, N, mt, "cluster4", grid);
     const bool pdl = pdl_enabled();
@@ -1405,9 +1408,12 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   p.err = d.err_word;
   p.w_reuse = m_tiles_run > 1 ? 1 : 0;
   const uint32_t bn = data_parallel ? 224u : uint32_t(kBN);
-  const CUtensorMap* tw = tensor_map_u8_2d(w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, bn);
-  const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt_run));
-  if (!tw || !tx) return FQ_ERR_CUDA;
+  CUtensorMap tw_map, tx_map;
+  if (!tensor_map_u8_2d(&tw_map, w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, bn) ||
+      !tensor_map_u8_2d(&tx_map, xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, uint32_t(mt_run)))
+    return FQ_ERR_CUDA;
+  const CUtensorMap* tw = &tw_map;
+  const CUtensorMap* tx = &tx_map;
   const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
   debug_schedule("w8a8_linear", M, K, N, mt_run, data_parallel ? "dp224" : (umma ? "umma" : "streamk"), grid);
   const bool pdl = pdl_enabled();
@@ -1526,9 +1532,12 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(
   p.offsets = offsets;
   p.E = int(E);
   p.w_reuse = 1;
-  const CUtensorMap* tw = tensor_map_u8_2d(w_enk, uint64_t(K), uint64_t(E * N), uint64_t(K), kBK, kBN);
-  const CUtensorMap* tx = tensor_map_u8_2d(xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, uint32_t(mt));
-  if (!tw || !tx) return FQ_ERR_CUDA;
+  CUtensorMap tw_map, tx_map;
+  if (!tensor_map_u8_2d(&tw_map, w_enk, uint64_t(K), uint64_t(E * N), uint64_t(K), kBK, kBN) ||
+      !tensor_map_u8_2d(&tx_map, xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, uint32_t(mt)))
+    return FQ_ERR_CUDA;
+  const CUtensorMap* tw = &tw_map;
+  const CUtensorMap* tx = &tx_map;
   const bool umma = forced_schedule() != SCHED_STREAMK;
   debug_schedule("w8a8_grouped_linear", R, K, N, mt, umma ? "umma" : "streamk", d.sm_count);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

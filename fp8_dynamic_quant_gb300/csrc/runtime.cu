@@ -102,8 +102,11 @@ constexpr int kMapCache = 256;
 thread_local MapEntry t_maps[kMapCache];
 }  // namespace
 
-const CUtensorMap* tensor_map_u8_2d(const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
-                                    uint32_t box_cols, uint32_t box_rows) {
+// The map is copied into *out: a pointer into the cache would be invalidated
+// by the next lookup that hashes to the same slot (a caller holding the weight
+// map while encoding the activation map would then launch with the wrong one).
+bool tensor_map_u8_2d(CUtensorMap* out, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
+                      uint32_t box_cols, uint32_t box_rows) {
   int dev = 0;
   cudaGetDevice(&dev);
   uint64_t h = reinterpret_cast<uintptr_t>(ptr) >> 4;
@@ -112,10 +115,12 @@ const CUtensorMap* tensor_map_u8_2d(const void* ptr, uint64_t cols, uint64_t row
   h ^= h >> 29;
   MapEntry& e = t_maps[h % kMapCache];
   if (e.valid && e.ptr == ptr && e.cols == cols && e.rows == rows && e.pitch == pitch &&
-      e.box_cols == box_cols && e.box_rows == box_rows && e.dev == dev)
-    return &e.map;
+      e.box_cols == box_cols && e.box_rows == box_rows && e.dev == dev) {
+    *out = e.map;
+    return true;
+  }
   EncodeTiledFn fn = encode_fn();
-  if (!fn) return nullptr;
+  if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {pitch};
   cuuint32_t box[2] = {box_cols, box_rows};
@@ -125,7 +130,7 @@ const CUtensorMap* tensor_map_u8_2d(const void* ptr, uint64_t cols, uint64_t row
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     e.valid = false;
-    return nullptr;
+    return false;
   }
   e.ptr = ptr;
   e.cols = cols;
@@ -135,7 +140,8 @@ const CUtensorMap* tensor_map_u8_2d(const void* ptr, uint64_t cols, uint64_t row
   e.box_rows = box_rows;
   e.dev = dev;
   e.valid = true;
-  return &e.map;
+  *out = e.map;
+  return true;
 }
 
 // One warp: lane 0 waits on an mbarrier that only it can complete.  The

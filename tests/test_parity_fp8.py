@@ -190,3 +190,28 @@ def test_einsum_repeatable(T):
     ys = [fq.fp8_group_einsum(xq, st, fq.SCALE_UE8M0_PACKED, wq, sw).view(torch.int16).clone() for _ in range(12)]
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
+
+
+def test_einsum_many_operand_addresses():
+    """Hundreds of calls whose weight and activation tensors sit at different
+    addresses: the encoded TMA descriptors are cached by address and shape, and
+    a weight descriptor must survive the activation lookup even when both keys
+    share a cache slot (with 256 slots, 400 calls make that near certain)."""
+    T, G, D, N = 4, 1, 256, 128
+    _, _, wq, sw = einsum_weights(G, N, D, 21)
+    x = synth.group_activations(T, G, D, 22)
+    xq, st = fq.quant_fp8_group_ue8m0_packed(bf16_to_dev(x))
+    ref = fq.fp8_group_einsum(xq, st, fq.SCALE_UE8M0_PACKED, wq, sw).view(torch.int16).clone()
+    wbytes, xbytes = wq.view(torch.uint8).reshape(-1), xq.view(torch.uint8).reshape(-1)
+    calls = 400
+    wbuf = torch.empty(wbytes.numel() + 16 * calls, dtype=torch.uint8, device="cuda")
+    xbuf = torch.empty(xbytes.numel() + 16 * calls, dtype=torch.uint8, device="cuda")
+    for i in range(calls):
+        wo, xo = 16 * i, 16 * ((7 * i) % calls)
+        wbuf[wo:wo + wbytes.numel()] = wbytes
+        xbuf[xo:xo + xbytes.numel()] = xbytes
+        wv = wbuf[wo:wo + wbytes.numel()].view(torch.float8_e4m3fn).view(G, N, D)
+        xv = xbuf[xo:xo + xbytes.numel()].view(torch.float8_e4m3fn).view(T, G, D)
+        y = fq.fp8_group_einsum(xv, st, fq.SCALE_UE8M0_PACKED, wv, sw)
+        assert torch.equal(y.view(torch.int16), ref), "call %d differs" % i
+    assert fq.device_error() == (0, 0)
