@@ -99,11 +99,14 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 }
 
 // Decoded activation scale from its stored word: a packed UE8M0 word holds
-// four k-blocks' exponent bytes; an fp32 word is the scale itself.
-__device__ __forceinline__ float decode_sx(uint32_t w, int fmt, int kb) {
-  if (fmt == FQ_SCALE_UE8M0_PACKED) {
-    const uint32_t u = (w >> (8 * (kb & 3))) & 0xFFu;
-    return u ? __uint_as_float(u << 23) : __uint_as_float(0x00400000u);  // 2^(u-127)
+// four k-blocks' exponent bytes, byte u meaning 2^(u-127) (u = 0 is the
+// subnormal 2^-127, kept exact so both formats give identical bits); an fp32
+// word is the scale itself.  `sel` picks byte kb % 4, zero-extended.
+template <int FMT>
+__device__ __forceinline__ float decode_sx(uint32_t w, uint32_t sel) {
+  if (FMT == FQ_SCALE_UE8M0_PACKED) {
+    const uint32_t u = __byte_perm(w, 0u, sel);
+    return __uint_as_float(u ? (u << 23) : 0x00400000u);
   }
   return __uint_as_float(w);
 }
@@ -136,7 +139,7 @@ __device__ __forceinline__ ETile etile(const Problem& p, int tile) {
   return t;
 }
 
-template <int MT, int CW>
+template <int MT, int CW, int FMT>
 __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     fp8_einsum_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
   using C = Cfg<MT, CW>;
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
         // this stage's token scale words and the tile's weight-block scale
         uint32_t* sc = scl + s * (MT + 4);
         if (lane == 0) cp_async4(sc + MT, p.sw + (int64_t(t.g) * KB + kb) * NB128 + (t.nb * BN) / 128);
-        if (p.fmt == FQ_SCALE_UE8M0_PACKED) {
+        if (FMT == FQ_SCALE_UE8M0_PACKED) {
           // packed words of 4 consecutive tokens are contiguous and 16-byte
           // aligned (the token dimension is padded to a multiple of 4)
           for (int c4 = lane; c4 < MT / 4; c4 += 32) {
@@ -301,13 +304,14 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
         }
         const uint32_t* sc = scl + s * (MT + 4);
         const float swv = __uint_as_float(sc[MT]);
+        const uint32_t sel = 0x4440u | uint32_t(kb & 3);  // byte kb % 4 of the word, zero-extended
         float sxs[NT][2];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int ml = 8 * j + frag_row(2 * c + hh);
-            sxs[j][hh] = (t.tt * MT + ml < p.T) ? decode_sx(sc[ml], p.fmt, kb) : 0.f;
+            sxs[j][hh] = (t.tt * MT + ml < p.T) ? decode_sx<FMT>(sc[ml], sel) : 0.f;
           }
         // The stage was read through the generic proxy (ld.shared); the next
         // TMA write into it goes through the async proxy.  Order the two
@@ -428,11 +432,11 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
 
 int pick_mt(int64_t T) { return T <= 8 ? 8 : (T <= 16 ? 16 : (T <= 32 ? 32 : 64)); }
 
-template <int MT, int CW>
-cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid, cudaStream_t s,
-                      bool pdl) {
+template <int MT, int CW, int FMT>
+cudaError_t launch_es1(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid, cudaStream_t s,
+                       bool pdl) {
   using Cf = Cfg<MT, CW>;
-  auto k = fp8_einsum_kernel<MT, CW>;
+  auto k = fp8_einsum_kernel<MT, CW, FMT>;
   static uint64_t attr_done = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -442,6 +446,13 @@ cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Proble
     attr_done |= 1ull << (dev & 63);
   }
   return launch(k, dim3(grid), dim3(Cf::THREADS), size_t(Cf::SMEM), s, pdl, *tw, *tx, p);
+}
+// The scale format is a compile-time parameter of the kernel.
+template <int MT, int CW>
+cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid, cudaStream_t s,
+                      bool pdl) {
+  return p.fmt == FQ_SCALE_UE8M0_PACKED ? launch_es1<MT, CW, FQ_SCALE_UE8M0_PACKED>(tw, tx, p, grid, s, pdl)
+                                        : launch_es1<MT, CW, FQ_SCALE_FP32>(tw, tx, p, grid, s, pdl);
 }
 }  // namespace es
 

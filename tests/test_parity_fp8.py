@@ -215,3 +215,27 @@ def test_einsum_many_operand_addresses():
         y = fq.fp8_group_einsum(xv, st, fq.SCALE_UE8M0_PACKED, wv, sw)
         assert torch.equal(y.view(torch.int16), ref), "call %d differs" % i
     assert fq.device_error() == (0, 0)
+
+
+def test_tiny_group_scale_byte_zero():
+    """A group whose absmax is tiny but nonzero clamps its exponent to -127
+    (byte 0) while its E4M3 codes stay nonzero: the quant must match the
+    oracle, and the einsum must decode byte 0 as 2^-127 in both scale formats."""
+    T, G, D, N = 2, 2, 256, 128
+    x = synth.group_activations(T, G, D, 31)
+    xf = codecs.bf16_to_f32(x).astype(np.float64)
+    xf[0, 0, :128] *= 2.0 ** -121 / np.abs(xf[0, 0, :128]).max()  # amax 2^-121: exponent clamps to -127
+    xf[1, 1, 128:] = 0.0            # and an all-zero group
+    xb = codecs.f64_to_bf16(xf)
+    xq, st = fq.quant_fp8_group_ue8m0_packed(bf16_to_dev(xb))
+    oxq, ost = of8.quant_fp8_group_ue8m0_packed(xb)
+    assert np.array_equal(st.cpu().numpy(), ost)
+    assert np.array_equal(e4m3_to_np(xq), oxq)
+    assert (ost.view(np.uint8).reshape(-1) == 0).any()
+    _, s32 = fq.quant_fp8_group_fp32(bf16_to_dev(xb))
+    owq, osw, wq, sw = einsum_weights(G, N, D, 32)
+    yp = fq.fp8_group_einsum(xq, st, fq.SCALE_UE8M0_PACKED, wq, sw)
+    yf = fq.fp8_group_einsum(xq, s32, fq.SCALE_FP32, wq, sw)
+    assert torch.equal(yp.view(torch.int16), yf.view(torch.int16))
+    want = of8.fp8_group_einsum(oxq, of8.unpack_scales(ost, T, D // 128), owq, osw)
+    assert within_tol(bf16_to_np(yp), want)
