@@ -65,7 +65,15 @@ def quant_fp8_group(x_bf16):
     Returns (xq uint8 E4M3 codes [T, G, D], e int32 exponents [T, G, NG]).
     q = E4M3_RN_satfinite(x * 2**-e); x * 2**-e is exact in float64.
     """
-    x = bf16_to_f32(np.asarray(x_bf16, np.uint16)).astype(np.float64)
+    return quant_fp8_group_values(bf16_to_f32(np.asarray(x_bf16, np.uint16)).astype(np.float64))
+
+
+def quant_fp8_group_values(x):
+    """The group rule on exact values x[T, G, D] (float64 holding bf16 or fp32
+    numbers).  ue8m0_exponent stays exact for fp32 absmax: a 24-bit value
+    divided by 448 = 7 * 2**6 lies at least 2**-26 (relative) away from a
+    power of two unless it equals one, far above float64's 2**-53 rounding."""
+    x = np.asarray(x, dtype=np.float64)
     T, G, D = x.shape
     NG, _, _ = packed_dims(T, D)
     xg = x.reshape(T, G, NG, GROUP)

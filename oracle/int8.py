@@ -28,7 +28,13 @@ def dynamic_quant_int8(x_bf16):
     [W8A8] section 1 (npu_dynamic_quant: INT8 X + per-token scale) and
     section 2 (one row = the last dimension, one token per row).
     """
-    x = bf16_to_f32(np.asarray(x_bf16, dtype=np.uint16))
+    return quant_int8_rows(bf16_to_f32(np.asarray(x_bf16, dtype=np.uint16)))
+
+
+def quant_int8_rows(x):
+    """The per-token INT8 rule on fp32 values x[M, K] (bf16 inputs widen
+    exactly; the RMSNorm producer feeds its fp32 rows here)."""
+    x = np.asarray(x, dtype=np.float32)
     if x.ndim != 2:
         raise ValueError("X must be [M, K]")
     M, K = x.shape
