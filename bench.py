@@ -441,6 +441,53 @@ def other_configs(fq, synth, torch, dev, bf, l2, hbm_peak):
                        "control_quant_fp32_repack_einsum_us": round(t_control, 2)}
     res["fp8_group_einsum_G8_D4096_N1024"] = ein
     del wq, sw
+    # --- RMSNorm fused with the INT8 per-token / FP8 per-group quant, K = 4096
+    K = 4096
+    gam = bf(synth.activations(1, K, SEED + 60)[0])
+    rq = {}
+    for M in [1, 4, 16, 64, 16384]:
+        copies = max(1, min(8, -(-2 * l2 // (2 * M * K))))
+        xs = [bf(synth.activations(M, K, SEED + 61 + c)) for c in range(copies)]
+        xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        sx = torch.empty((M,), dtype=torch.float32, device=dev)
+        x8 = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+        s8 = torch.empty((1, (K // 128 + 3) // 4, (M + 3) // 4 * 4), dtype=torch.int32, device=dev)
+        R = max(copies, 8)
+        ui = time_graph(torch, lambda: [fq.rmsnorm_quant_int8(xs[i % copies], gam, 1e-6, xq, sx) for i in range(R)],
+                        calls=R)
+        uf = time_graph(torch, lambda: [fq.rmsnorm_quant_fp8_ue8m0_packed(xs[i % copies], gam, 1e-6, x8, s8)
+                                        for i in range(R)], calls=R)
+        bi = 3 * M * K + 2 * K + 4 * M
+        bfp = 3 * M * K + 2 * K + 4 * s8.numel()
+        rq[str(M)] = {"int8_us": round(ui, 2), "int8_GBps": round(bi / (ui * 1e-6) / 1e9, 1),
+                      "fp8_us": round(uf, 2), "fp8_GBps": round(bfp / (uf * 1e-6) / 1e9, 1),
+                      "int8_frac_hbm": round(bi / (ui * 1e-6) / 1e9 / hbm_peak, 3)}
+        del xs
+    res["rmsnorm_quant_K4096"] = rq
+    # --- expert-local M_e sweep of the grouped W8A8 linear: 16 experts of M_e rows each
+    Ex = 16
+    me_res = {}
+    for (K, N, name) in [(4096, 4096, "W13_K4096_N4096"), (2048, 4096, "W2_K2048_N4096")]:
+        wg = synth.uniform_int8_device((Ex, N, K), SEED + 70 + K, dev)
+        swg = synth.uniform_f32_device((Ex, N), 1e-3, 1e-2, SEED + 71 + K, dev)
+        row = {}
+        for Me in [1, 2, 4, 8, 16, 32, 64, 96, 127, 128, 129, 160, 192, 256]:
+            R = Ex * Me
+            xg = synth.uniform_int8_device((R, K), SEED + 72 + Me, dev)
+            sg = synth.uniform_f32_device((R,), 1e-3, 1e-2, SEED + 73 + Me, dev)
+            offs = torch.arange(0, R + 1, Me, dtype=torch.int32, device=dev)
+            yg = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+            wsg = fq.new_workspace(fq.workspace_bytes(fq.OP_W8A8_GROUPED_LINEAR, R, K, N, Ex), dev)
+            us = time_graph(torch, lambda: fq.w8a8_grouped_linear(xg, sg, offs, wg, swg, y=yg, ws=wsg), reps=3,
+                            calls=1)
+            nbytes = Ex * N * K + 4 * Ex * N + R * K + 4 * R + 2 * R * N
+            row[str(Me)] = {"us": round(us, 1), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                            "TOPS": round(2.0 * R * N * K / (us * 1e-6) / 1e12, 1)}
+            del xg, yg, wsg
+        me_res[name] = row
+        del wg, swg
+    res["grouped_w8a8_Me_sweep_16_experts"] = me_res
+    torch.cuda.empty_cache()
     # --- MoE expert chain: 256 tokens, hidden 4096, 256 experts, top-8 Zipf(1.1), intermediate 2048
     T, topk, E, H, I = 256, 8, 256, 4096, 2048
     c = synth.moe_case(T, topk, E, H, I, SEED + 4, with_weights=False)

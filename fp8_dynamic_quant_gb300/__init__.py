@@ -14,7 +14,8 @@ __all__ = [
     "FqError", "lib", "lib_path", "dynamic_quant_int8", "w8a8_linear", "w8a8_quant_linear",
     "quant_fp8_group_ue8m0_packed", "quant_fp8_group_fp32", "pack_scales_ue8m0", "quantize_weight_fp8_block",
     "fp8_group_einsum", "scale_view", "moe_sort", "moe_gather_rows_i8", "w8a8_grouped_linear",
-    "swiglu_quant_int8", "moe_combine", "device_error", "selftest_wait_timeout", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
+    "swiglu_quant_int8", "moe_combine", "device_error", "selftest_wait_timeout", "rmsnorm_quant_int8",
+    "rmsnorm_quant_fp8_ue8m0_packed", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
     "OP_W8A8_LINEAR", "OP_W8A8_QUANT_LINEAR", "OP_FP8_GROUP_EINSUM", "OP_MOE_SORT", "OP_W8A8_GROUPED_LINEAR",
 ]
 
@@ -32,6 +33,8 @@ _SIGS = {
     "fq_last_cuda_error": ([], _I32),
     "fq_device_error": ([_P, _U32P], _I32),
     "fq_selftest_wait_timeout": ([ctypes.c_uint64, _I32, _P], _I32),
+    "rmsnorm_quant_int8": ([_P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P], _I32),
+    "rmsnorm_quant_fp8_ue8m0_packed": ([_P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P], _I32),
     "fq_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64], _SZ),
     "dynamic_quant_int8": ([_P, _I64, _I64, _P, _P, _P], _I32),
     "w8a8_linear": ([_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P], _I32),
@@ -137,6 +140,34 @@ def selftest_wait_timeout(budget_ns=1_000_000, arrive=False):
     with arrive=False the wait runs out and device_error() then reports
     FQ_ERR_DEVICE_TIMEOUT."""
     _check("fq_selftest_wait_timeout", lib().fq_selftest_wait_timeout(int(budget_ns), 1 if arrive else 0, _stream()))
+
+
+# ---------------------------------------------------------------- RMSNorm + quant
+
+def rmsnorm_quant_int8(x, gamma, eps=1e-6, xq=None, sx=None):
+    """x bf16 [M, K], gamma bf16 [K] -> (xq int8 [M, K], sx fp32 [M]) of RMSNorm(x)."""
+    _cuda(x, torch.bfloat16, "x")
+    _cuda(gamma, torch.bfloat16, "gamma")
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.int8, device=x.device) if xq is None else xq
+    sx = torch.empty((M,), dtype=torch.float32, device=x.device) if sx is None else sx
+    _check("rmsnorm_quant_int8", lib().rmsnorm_quant_int8(_ptr(x), _ptr(gamma), float(eps), M, K, _ptr(xq),
+                                                          _ptr(sx), _stream()))
+    return xq, sx
+
+
+def rmsnorm_quant_fp8_ue8m0_packed(x, gamma, eps=1e-6, xq=None, s_packed=None):
+    """x bf16 [T, K], gamma bf16 [K] -> (xq float8_e4m3fn [T, K], int32 [1, P, Ta]) of RMSNorm(x)."""
+    _cuda(x, torch.bfloat16, "x")
+    _cuda(gamma, torch.bfloat16, "gamma")
+    T, K = x.shape
+    P, Ta = (K // 128 + 3) // 4, (T + 3) // 4 * 4
+    xq = torch.empty((T, K), dtype=torch.float8_e4m3fn, device=x.device) if xq is None else xq
+    s_packed = torch.empty((1, P, Ta), dtype=torch.int32, device=x.device) if s_packed is None else s_packed
+    _check("rmsnorm_quant_fp8_ue8m0_packed",
+           lib().rmsnorm_quant_fp8_ue8m0_packed(_ptr(x), _ptr(gamma), float(eps), T, K, _ptr(xq), _ptr(s_packed),
+                                                _stream()))
+    return xq, s_packed
 
 
 # ---------------------------------------------------------------- INT8 path

@@ -330,6 +330,192 @@ __global__ void __launch_bounds__(256) quant_fp8_group_kernel(const uint4* __res
   }
 }
 
+// ---------------------------------------------------------------- RMSNorm + quant producer
+//
+// "Reshaping LLM inference dataflow: DeepSeek V4 950" section 2.3, first
+// fusion: normalise in registers and write only the quantized activation.
+// One CTA (256 threads) per row, each thread holding VPT 16-byte vectors.
+//   ss = sum x^2, rounded once to fp64 from an integer sum: a bf16 value is
+//        an 8-bit integer mantissa times a power of two, so every x^2 is a
+//        16-bit integer shifted by twice its exponent; aligned to the row's
+//        largest exponent with a 96-bit window the terms add exactly in a
+//        128-bit integer, and bits below the window only set a sticky bit
+//        (their total is below 2^-82 of the sum; the sticky bit keeps the
+//        fp64 rounding of ties exact);
+//   r  = fp32(1 / sqrt(ss / K + eps)) in IEEE fp64 steps (r = 0 if the
+//        argument is 0);
+//   y  = fp32(fp32(x * r) * gamma), then the INT8 per-token rule or the FP8
+//        per-128-group rule with packed UE8M0 scales (one outer group).
+typedef unsigned __int128 u128;
+
+// x^2 of a bf16-valued float in units of 2^(2*(emax - 134) - 96), where emax
+// is the row's largest biased exponent (subnormals count as exponent 1).
+// Bits that fall below the window are dropped and reported in `sticky`; the
+// caller ORs them into the lowest unit of the sum, which lies far below the
+// fp64 rounding position, so a rounding tie is broken as the exact sum would.
+__device__ __forceinline__ u128 sq_units(float v, int emax, uint32_t& sticky) {
+  const uint32_t b = __float_as_uint(v);
+  const int ex = int((b >> 23) & 0xFFu);
+  const uint32_t m = ((b >> 16) & 0x7Fu) | (ex ? 0x80u : 0u);  // the 8-bit integer mantissa
+  const int d = 2 * (emax - (ex ? ex : 1));
+  const uint64_t m2 = uint64_t(m) * m;  // < 2^16
+  if (d <= 96) return u128(m2) << (96 - d);
+  const int sh = d - 96;
+  if (sh >= 16) {
+    sticky |= (m2 != 0);
+    return 0;
+  }
+  sticky |= ((m2 & ((1ull << sh) - 1)) != 0);
+  return u128(m2 >> sh);
+}
+
+// Correctly rounded fp64 value of S * 2^k (S > 0): the top 64 bits of S with
+// a sticky bit for anything below, converted with one rounding, then an
+// exact power-of-two scaling.
+__device__ __forceinline__ double u128_to_f64_scaled(u128 S, int k) {
+  const uint64_t hi = uint64_t(S >> 64), lo = uint64_t(S);
+  uint64_t top;
+  int shift;
+  if (hi) {
+    const int lz = __clzll(hi);
+    shift = 64 - lz;  // bits dropped below the top 64
+    top = (hi << lz) | (lz ? (lo >> (64 - lz)) : 0ull);
+    const uint64_t rest = lz ? (lo << lz) : lo;
+    if (rest) top |= 1ull;
+  } else {
+    top = lo;
+    shift = 0;
+  }
+  const double t = __ull2double_rn(top);
+  const int e = k + shift;  // within fp64's normal range for any bf16 row
+  return __dmul_rn(t, __longlong_as_double(int64_t(e + 1023) << 52));
+}
+
+template <int VPT, bool FP8>
+__global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma,
+                                                             float eps, int64_t rows, int64_t T, int64_t K8,
+                                                             uint2* __restrict__ q, float* __restrict__ sx,
+                                                             int32_t* __restrict__ s_packed, int P, int Ta) {
+  __shared__ uint64_t red_hi[8], red_lo[8];
+  __shared__ uint32_t red_sticky[8];
+  __shared__ float red[32];
+  __shared__ float s_r;
+  __shared__ uint8_t s_bytes[(FP8 ? VPT * 256 / 16 : 1) + 4];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    if (FP8 && row >= T) {  // token padding of the packed scales: zero words
+      for (int p = tid; p < P; p += 256) s_packed[int64_t(p) * Ta + row] = 0;
+      continue;
+    }
+    const uint4* xr = x + row * K8;
+    float f[VPT][8];
+    float xmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * 256;
+      if (idx < K8) {
+        unpack8(ld_stream(xr + idx), f[i]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[i][k] = 0.0f;
+      }
+      xmax = fmaxf(xmax, absmax8(f[i]));
+    }
+    xmax = block_max(xmax, red);
+    const int emax_raw = int((__float_as_uint(xmax) >> 23) & 0xFFu);
+    const int emax = emax_raw ? emax_raw : 1;
+    u128 acc = 0;
+    uint32_t sticky = 0;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc += sq_units(f[i][k], emax, sticky);
+    sticky = __any_sync(0xFFFFFFFFu, sticky != 0);
+    uint64_t ahi = uint64_t(acc >> 64), alo = uint64_t(acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const u128 other = (u128(__shfl_xor_sync(0xFFFFFFFFu, ahi, o)) << 64) | __shfl_xor_sync(0xFFFFFFFFu, alo, o);
+      const u128 sum = ((u128(ahi) << 64) | alo) + other;
+      ahi = uint64_t(sum >> 64);
+      alo = uint64_t(sum);
+    }
+    if (lane == 0) {
+      red_hi[warp] = ahi;
+      red_lo[warp] = alo;
+      red_sticky[warp] = sticky;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      u128 S = 0;
+      uint32_t st_any = 0;
+      for (int w = 0; w < 8; ++w) {
+        S += (u128(red_hi[w]) << 64) | red_lo[w];
+        st_any |= red_sticky[w];
+      }
+      if (st_any) S |= 1u;
+      const double ss = S == 0 ? 0.0 : u128_to_f64_scaled(S, 2 * (emax - 134) - 96);
+      const double u = __dadd_rn(__ddiv_rn(ss, double(K8 * 8)), double(eps));
+      s_r = (u == 0.0) ? 0.0f : __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(u)));
+    }
+    __syncthreads();
+    const float r = s_r;
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * 256;
+      if (idx < K8) {
+        float g[8];
+        unpack8(__ldg(gamma + idx), g);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[i][k] = __fmul_rn(__fmul_rn(f[i][k], r), g[k]);
+      }
+      if (!FP8) amax = fmaxf(amax, absmax8(f[i]));
+    }
+    uint2* qr = q + row * K8;
+    if (!FP8) {
+      amax = block_max(amax, red);
+      const float sc = __fdiv_rn(amax, 127.0f);
+      const float inv = __frcp_rn(sc);
+      if (tid == 0) sx[row] = sc;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int64_t idx = tid + int64_t(i) * 256;
+        if (idx < K8) qr[idx] = quant8_i8(f[i], sc, inv);
+      }
+    } else {
+      // a 128-element group is 16 consecutive vectors: 16 consecutive threads
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int64_t idx = tid + int64_t(i) * 256;
+        float ga = absmax8(f[i]);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ga = fmaxf(ga, __shfl_xor_sync(0xFFFFFFFFu, ga, o));
+        if (idx < K8) {
+          const int e = ue8m0_exp(ga);
+          const float sc = exp2_int(-e);
+          uint2 o;
+          o.x = e4m3x4(f[i][0] * sc, f[i][1] * sc, f[i][2] * sc, f[i][3] * sc);
+          o.y = e4m3x4(f[i][4] * sc, f[i][5] * sc, f[i][6] * sc, f[i][7] * sc);
+          qr[idx] = o;
+          if ((idx & 15) == 0) s_bytes[idx >> 4] = uint8_t(e + 127);
+        }
+      }
+      __syncthreads();
+      const int NG = int(K8 >> 4);
+      for (int p = tid; p < P; p += 256) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (4 * p + b < NG) w |= uint32_t(s_bytes[4 * p + b]) << (8 * b);
+        s_packed[int64_t(p) * Ta + row] = int32_t(w);
+      }
+    }
+    __syncthreads();  // shared scratch is reused by the next row
+  }
+}
+
 // fp32 power-of-two scales [T, G, NG] -> packed int32 [G, P, Ta]; one thread per word.
 __global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restrict__ s, int T, int G, int NG, int P,
                                                            int Ta, int32_t* __restrict__ out) {
@@ -549,4 +735,56 @@ extern "C" __attribute__((visibility("default"))) fq_status fq_quantize_weight_f
   return cuda_status(launch(quantize_weight_fp8_kernel, int(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream),
                             false, reinterpret_cast<const float4*>(w_gnd), int(G), int(N), int(D),
                             reinterpret_cast<uint32_t*>(wq), sw_blk));
+}
+
+static fq_status rmsnorm_common(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M, int64_t K, void* q,
+                                float* sx, int32_t* s_packed, fq_stream_t stream, bool fp8) {
+  if (!(eps >= 0.0f) || !(eps <= 3.4e38f)) return FQ_ERR_ARG;  // finite, non-negative
+  if (M < 0 || K < 0 || K % (fp8 ? 128 : 16) || K > 16384 || M > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
+  if (M == 0 || K == 0) return FQ_OK;
+  if (!x || !gamma || !q || (fp8 ? !s_packed : !sx)) return FQ_ERR_NULL;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(q) || !aligned16(fp8 ? (const void*)s_packed : (const void*)sx))
+    return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  const int64_t K8 = K / 8;
+  const int64_t rows = fp8 ? (M + 3) / 4 * 4 : M;
+  const int P = int((K / 128 + 3) / 4), Ta = int((M + 3) / 4 * 4);
+  const int grid = grid_for(rows, 1, d.sm_count, 8);
+  const int64_t vpt = (K8 + 255) / 256;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool pdl = pdl_enabled();
+  auto xp = reinterpret_cast<const uint4*>(x);
+  auto gp = reinterpret_cast<const uint4*>(gamma);
+  auto qp = reinterpret_cast<uint2*>(q);
+  cudaError_t e;
+#define FQ_RMS_LAUNCH(V)                                                                                          \
+  (fp8 ? launch(rmsnorm_quant_kernel<V, true>, grid, 256, 0, s, pdl, xp, gp, eps, rows, M, K8, qp, sx, s_packed, P, \
+                Ta)                                                                                                \
+       : launch(rmsnorm_quant_kernel<V, false>, grid, 256, 0, s, pdl, xp, gp, eps, rows, M, K8, qp, sx, s_packed,  \
+                P, Ta))
+  if (vpt <= 1)
+    e = FQ_RMS_LAUNCH(1);
+  else if (vpt <= 2)
+    e = FQ_RMS_LAUNCH(2);
+  else if (vpt <= 4)
+    e = FQ_RMS_LAUNCH(4);
+  else
+    e = FQ_RMS_LAUNCH(8);
+#undef FQ_RMS_LAUNCH
+  return cuda_status(e);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status rmsnorm_quant_int8(const uint16_t* x, const uint16_t* gamma,
+                                                                               float eps, int64_t M, int64_t K,
+                                                                               int8_t* xq, float* sx,
+                                                                               fq_stream_t stream) {
+  return rmsnorm_common(x, gamma, eps, M, K, xq, sx, nullptr, stream, false);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status rmsnorm_quant_fp8_ue8m0_packed(
+    const uint16_t* x, const uint16_t* gamma, float eps, int64_t T, int64_t K, uint8_t* xq, int32_t* s_packed,
+    fq_stream_t stream) {
+  return rmsnorm_common(x, gamma, eps, T, K, xq, nullptr, s_packed, stream, true);
 }

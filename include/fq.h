@@ -233,6 +233,32 @@ fq_status fp8_group_einsum(const uint8_t* xq, const void* sx, int fmt,
                            const uint8_t* w_gnd, const float* sw_blk, int64_t N, uint16_t* y,
                            void* ws, size_t ws_bytes, fq_stream_t stream);
 
+/* ------------------------------------------------- RMSNorm + quant producer */
+
+/* RMSNorm fused with the activation quant, the producer of a linear's
+ * quantized input ([DF] section 2.3, first fusion: the normalised row stays
+ * in registers and only the quantized activation is written; [W8A8]
+ * section 1: the linear consumes the ready (int8, scale) tuple).
+ *   x     : bf16 [M, K] (or [T, K])   in, row-major
+ *   gamma : bf16 [K]                  in
+ *   eps   : finite, >= 0              (else FQ_ERR_ARG)
+ * Per row: ss = sum x^2 exactly, rounded once to fp64;
+ *          r  = fp32(1 / sqrt(ss / K + eps)) (fp64 steps; 0 if the argument is 0);
+ *          y  = fp32(fp32(x * r) * gamma), kept in fp32 (never rounded to bf16).
+ * rmsnorm_quant_int8: the per-token INT8 rule of dynamic_quant_int8 on y:
+ *   xq int8 [M, K], sx fp32 [M].  K % 16 == 0.
+ * rmsnorm_quant_fp8_ue8m0_packed: the per-128-group rule of
+ *   quant_fp8_group_ue8m0_packed on y with one outer group (G = 1, D = K):
+ *   xq E4M3 [T, K], s_packed int32 [1, ceil(K/512), align_up(T, 4)] (unused
+ *   pack bytes and token-padding words written as zero).  K % 128 == 0.
+ * Both: K <= 16384; all pointers 16-byte aligned; asynchronous on `stream`.
+ * Rows whose r overflows fp32 (eps == 0 and ss / K below about 2^-254) are
+ * outside the contract. */
+fq_status rmsnorm_quant_int8(const uint16_t* x, const uint16_t* gamma, float eps, int64_t M, int64_t K,
+                             int8_t* xq, float* sx, fq_stream_t stream);
+fq_status rmsnorm_quant_fp8_ue8m0_packed(const uint16_t* x, const uint16_t* gamma, float eps, int64_t T, int64_t K,
+                                         uint8_t* xq, int32_t* s_packed, fq_stream_t stream);
+
 /* ------------------------------------------------------------------- MoE */
 
 /* Stable sort of the (token, slot) pairs of topk_ids [T, topk] by expert id.

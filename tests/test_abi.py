@@ -73,6 +73,15 @@ def test_host_validation_before_any_device_call(libfq):
     # misaligned pointers
     assert L.dynamic_quant_int8(ctypes.c_void_p(0x1008), 4, 4096, ctypes.c_void_p(0x2000),
                                 ctypes.c_void_p(0x3000), None) == 3
+    # RMSNorm + quant: eps must be finite and >= 0; K % 16 (INT8) / % 128 (FP8); K <= 16384
+    assert L.rmsnorm_quant_int8(None, None, -1.0, 4, 4096, None, None, None) == 9
+    assert L.rmsnorm_quant_int8(None, None, float("nan"), 4, 4096, None, None, None) == 9
+    assert L.rmsnorm_quant_int8(None, None, float("inf"), 4, 4096, None, None, None) == 9
+    assert L.rmsnorm_quant_int8(None, None, 1e-6, 4, 4100, None, None, None) == 2
+    assert L.rmsnorm_quant_int8(None, None, 1e-6, 4, 16400, None, None, None) == 2
+    assert L.rmsnorm_quant_fp8_ue8m0_packed(None, None, 1e-6, 4, 4112, None, None, None) == 2
+    assert L.rmsnorm_quant_int8(None, None, 1e-6, 0, 4096, None, None, None) == 0
+    assert L.rmsnorm_quant_int8(None, None, 1e-6, 4, 4096, None, None, None) == 1
 
 
 def test_workspace_sizing_without_device_is_zero():
