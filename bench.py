@@ -464,6 +464,39 @@ def other_configs(fq, synth, torch, dev, bf, l2, hbm_peak):
                       "int8_frac_hbm": round(bi / (ui * 1e-6) / 1e9 / hbm_peak, 3)}
         del xs
     res["rmsnorm_quant_K4096"] = rq
+    # --- 32-element block-scaled FP8 (MXFP8-like): producer and tensor-core block-scaled linear
+    mxr = {}
+    for (K, N) in LINEARS:
+        ncp = max(2, -(-2 * l2 // (K * N)) + 1)
+        wl = []
+        for c in range(ncp):
+            wb = (torch.randn((N, K), generator=torch.Generator(device=dev).manual_seed(SEED + 80 + c), device=dev)
+                  * 0.02).to(torch.bfloat16)
+            wl.append(fq.quant_mxfp8(wb))
+            del wb
+        row = {}
+        for M in [1, 4, 16, 64, 128]:
+            xb = bf(synth.activations(M, K, SEED + 81 + M))
+            qx, sxb = fq.quant_mxfp8(xb)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            wsm = fq.new_workspace(fq.workspace_bytes(fq.OP_MXFP8_LINEAR, M, K, N), dev)
+            us = time_graph(torch, lambda: [fq.mxfp8_linear(qx, sxb, wl[c][0], wl[c][1], y=y, ws=wsm)
+                                            for c in range(ncp)], calls=ncp)
+            nbytes = N * K + N * K // 32 + M * K + M * K // 32 + 2 * M * N
+            row[str(M)] = {"us": round(us, 2), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                           "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 3)}
+        mxr["linear_K%d_N%d" % (K, N)] = row
+        del wl
+    M, K = 16384, 4096
+    xs = [bf(synth.activations(M, K, SEED + 90 + c)) for c in range(2)]
+    q8 = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    sfb = torch.empty(((M + 127) // 128, K // 128, 512), dtype=torch.uint8, device=dev)
+    us = time_graph(torch, lambda: [fq.quant_mxfp8(xs[i % 2], q8, sfb) for i in range(4)], calls=4)
+    nbytes = 3 * M * K + M * K // 32
+    mxr["quant_M16384_K4096"] = {"us": round(us, 2), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                 "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm_peak, 3)}
+    del xs
+    res["mxfp8_block32"] = mxr
     # --- expert-local M_e sweep of the grouped W8A8 linear: 16 experts of M_e rows each
     Ex = 16
     me_res = {}

@@ -15,13 +15,14 @@ __all__ = [
     "quant_fp8_group_ue8m0_packed", "quant_fp8_group_fp32", "pack_scales_ue8m0", "quantize_weight_fp8_block",
     "fp8_group_einsum", "scale_view", "moe_sort", "moe_gather_rows_i8", "w8a8_grouped_linear",
     "swiglu_quant_int8", "moe_combine", "device_error", "selftest_wait_timeout", "rmsnorm_quant_int8",
-    "rmsnorm_quant_fp8_ue8m0_packed", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
+    "rmsnorm_quant_fp8_ue8m0_packed", "quant_mxfp8", "mxfp8_linear", "OP_MXFP8_LINEAR", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
     "OP_W8A8_LINEAR", "OP_W8A8_QUANT_LINEAR", "OP_FP8_GROUP_EINSUM", "OP_MOE_SORT", "OP_W8A8_GROUPED_LINEAR",
 ]
 
 SCALE_UE8M0_PACKED = 0
 SCALE_FP32 = 1
 OP_W8A8_LINEAR, OP_W8A8_QUANT_LINEAR, OP_FP8_GROUP_EINSUM, OP_MOE_SORT, OP_W8A8_GROUPED_LINEAR = 1, 2, 3, 4, 5
+OP_MXFP8_LINEAR = 6
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libfq.so")
@@ -35,6 +36,8 @@ _SIGS = {
     "fq_selftest_wait_timeout": ([ctypes.c_uint64, _I32, _P], _I32),
     "rmsnorm_quant_int8": ([_P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P], _I32),
     "rmsnorm_quant_fp8_ue8m0_packed": ([_P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P], _I32),
+    "quant_mxfp8": ([_P, _I64, _I64, _P, _P, _P], _I32),
+    "mxfp8_linear": ([_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P], _I32),
     "fq_workspace_bytes": ([_I32, _I64, _I64, _I64, _I64], _SZ),
     "dynamic_quant_int8": ([_P, _I64, _I64, _P, _P, _P], _I32),
     "w8a8_linear": ([_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P], _I32),
@@ -168,6 +171,32 @@ def rmsnorm_quant_fp8_ue8m0_packed(x, gamma, eps=1e-6, xq=None, s_packed=None):
            lib().rmsnorm_quant_fp8_ue8m0_packed(_ptr(x), _ptr(gamma), float(eps), T, K, _ptr(xq), _ptr(s_packed),
                                                 _stream()))
     return xq, s_packed
+
+
+# ---------------------------------------------------------------- 32-element block-scaled FP8
+
+def quant_mxfp8(x, q=None, sf=None):
+    """x bf16 [R, K] -> (q float8_e4m3fn [R, K], blocked scales uint8 [ceil(R/128), K/128, 512])."""
+    _cuda(x, torch.bfloat16, "x")
+    R, K = x.shape
+    q = torch.empty((R, K), dtype=torch.float8_e4m3fn, device=x.device) if q is None else q
+    sf = torch.empty(((R + 127) // 128, K // 128, 512), dtype=torch.uint8, device=x.device) if sf is None else sf
+    _check("quant_mxfp8", lib().quant_mxfp8(_ptr(x), R, K, _ptr(q), _ptr(sf), _stream()))
+    return q, sf
+
+
+def mxfp8_linear(xq, xsf, wq, wsf, y=None, ws=None):
+    """E4M3 xq [M, K] + blocked scales, E4M3 wq [N, K] + blocked scales -> bf16 y [M, N]."""
+    _cuda(xq, torch.float8_e4m3fn, "xq"), _cuda(wq, torch.float8_e4m3fn, "wq")
+    _cuda(xsf, torch.uint8, "xsf"), _cuda(wsf, torch.uint8, "wsf")
+    M, K = xq.shape
+    N = wq.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
+    nb = workspace_bytes(OP_MXFP8_LINEAR, M, K, N)
+    ws = _workspace(nb, xq.device, ws)
+    _check("mxfp8_linear", lib().mxfp8_linear(_ptr(xq), _ptr(xsf), M, K, _ptr(wq), _ptr(wsf), N, _ptr(y), _ptr(ws),
+                                              ws.numel() * ws.element_size(), _stream()))
+    return y
 
 
 # ---------------------------------------------------------------- INT8 path

@@ -516,6 +516,55 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const uint4* __restr
   }
 }
 
+// ---------------------------------------------------------------- 32-element block-scaled FP8
+//
+// "Reshaping LLM inference dataflow: DeepSeek V4 950" section 2.1: 32
+// elements share one 8-bit (UE8M0) scale with E4M3 payloads.  One thread per
+// 8-element vector, 4 consecutive lanes per 32-element block (a shuffle
+// gives the block absmax).  The scale bytes are written in the blocked layout
+// the linear's tensor-core scale copy reads: for every 128 rows x 128 K one
+// 512-byte chunk, row r's byte for K block b at
+// (r % 32) * 16 + ((r % 128) / 32) * 4 + b % 4.
+__global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint4* __restrict__ x, int64_t R, int64_t K8,
+                                                          uint2* __restrict__ q, uint8_t* __restrict__ sf) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int64_t total = R * K8, KB = K8 / 16;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t span = (total + 31) / 32 * 32;  // whole warps stay in the loop together
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v - threadIdx.x % 32 < span; v += stride) {
+    const bool ok = v < total;
+    float f[8];
+    if (ok) {
+      unpack8(ld_stream(x + v), f);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = 0.0f;
+    }
+    float amax = absmax8(f);
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    if (ok) {
+      const int e = ue8m0_exp(amax);
+      const float sc = exp2_int(-e);
+      uint2 o;
+      o.x = e4m3x4(f[0] * sc, f[1] * sc, f[2] * sc, f[3] * sc);
+      o.y = e4m3x4(f[4] * sc, f[5] * sc, f[6] * sc, f[7] * sc);
+      q[v] = o;
+      if ((v & 3) == 0) {
+        const int64_t r = v / K8, b = (v - r * K8) >> 2;
+        sf[((r >> 7) * KB + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3)] = uint8_t(e + 127);
+      }
+    }
+  }
+  // rows R .. 128*ceil(R/128)-1 of the last chunk row hold zero bytes
+  const int64_t pad_rows = (R + 127) / 128 * 128 - R;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < pad_rows * KB * 4; i += stride) {
+    const int64_t r = R + i / (KB * 4), b = i % (KB * 4);
+    sf[((r >> 7) * KB + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3)] = 0;
+  }
+}
+
 // fp32 power-of-two scales [T, G, NG] -> packed int32 [G, P, Ta]; one thread per word.
 __global__ void __launch_bounds__(256) pack_scales_kernel(const float* __restrict__ s, int T, int G, int NG, int P,
                                                            int Ta, int32_t* __restrict__ out) {
@@ -787,4 +836,20 @@ extern "C" __attribute__((visibility("default"))) fq_status rmsnorm_quant_fp8_ue
     const uint16_t* x, const uint16_t* gamma, float eps, int64_t T, int64_t K, uint8_t* xq, int32_t* s_packed,
     fq_stream_t stream) {
   return rmsnorm_common(x, gamma, eps, T, K, xq, nullptr, s_packed, stream, true);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status quant_mxfp8(const uint16_t* x, int64_t R, int64_t K,
+                                                                        uint8_t* q, uint8_t* sf_blocked,
+                                                                        fq_stream_t stream) {
+  if (R < 0 || K < 0 || K % 128 || K > (int64_t(1) << 20) || R > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
+  if (R == 0 || K == 0) return FQ_OK;
+  if (!x || !q || !sf_blocked) return FQ_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf_blocked)) return FQ_ERR_ALIGN;
+  DevInfo d;
+  fq_status st = device_info(&d);
+  if (st != FQ_OK) return st;
+  const int64_t K8 = K / 8;
+  const int grid = grid_for(R * K8, 256, d.sm_count, 8);
+  return cuda_status(launch(quant_mxfp8_kernel, grid, 256, 0, reinterpret_cast<cudaStream_t>(stream), pdl_enabled(),
+                            reinterpret_cast<const uint4*>(x), R, K8, reinterpret_cast<uint2*>(q), sf_blocked));
 }

@@ -217,6 +217,7 @@ extern "C" __attribute__((visibility("default"))) size_t fq_workspace_bytes(int 
     case FQ_OP_FP8_GROUP_EINSUM: return ws_fp8_group_einsum(a, b, c, d);
     case FQ_OP_MOE_SORT: return 256;
     case FQ_OP_W8A8_GROUPED_LINEAR: return ws_w8a8_grouped_linear(a, b, c, d);
+    case FQ_OP_MXFP8_LINEAR: return ws_mxfp8_linear(a, b, c);
     default: return 0;
   }
 }

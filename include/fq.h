@@ -100,13 +100,15 @@ fq_status fq_selftest_wait_timeout(uint64_t budget_ns, int arrive, fq_stream_t s
  *   FQ_OP_FP8_GROUP_EINSUM:                       (T, D, N, G)
  *   FQ_OP_MOE_SORT:                               (T*topk, unused, unused, E)
  *   FQ_OP_W8A8_GROUPED_LINEAR:                    (R rows, K, N, E)
+ *   FQ_OP_MXFP8_LINEAR:                           (M, K, N, unused)
  * Returns 0 for an unknown op or invalid sizes. */
 typedef enum fq_op {
   FQ_OP_W8A8_LINEAR = 1,
   FQ_OP_W8A8_QUANT_LINEAR = 2,
   FQ_OP_FP8_GROUP_EINSUM = 3,
   FQ_OP_MOE_SORT = 4,
-  FQ_OP_W8A8_GROUPED_LINEAR = 5
+  FQ_OP_W8A8_GROUPED_LINEAR = 5,
+  FQ_OP_MXFP8_LINEAR = 6
 } fq_op;
 size_t fq_workspace_bytes(int op, int64_t a, int64_t b, int64_t c, int64_t d);
 
@@ -258,6 +260,33 @@ fq_status rmsnorm_quant_int8(const uint16_t* x, const uint16_t* gamma, float eps
                              int8_t* xq, float* sx, fq_stream_t stream);
 fq_status rmsnorm_quant_fp8_ue8m0_packed(const uint16_t* x, const uint16_t* gamma, float eps, int64_t T, int64_t K,
                                          uint8_t* xq, int32_t* s_packed, fq_stream_t stream);
+
+/* ------------------------------------------ 32-element block-scaled FP8 */
+
+/* MXFP8-like block scaling ([DF] section 2.1: every 32 elements share one
+ * 8-bit scale, E4M3 payloads); the per-128-group rule of
+ * quant_fp8_group_ue8m0_packed applied to 32-element blocks along K.
+ * Scale storage is blocked for the linear's tensor-core scale copy: for every
+ * 128 rows x 128 K one 512-byte chunk, chunk (r / 128, k / 128) at byte offset
+ * ((r / 128) * (K / 128) + k / 128) * 512; row r's byte for K block b = k / 32
+ * at (r % 32) * 16 + ((r % 128) / 32) * 4 + b % 4 within it; rows past R in
+ * the last chunk row are zero bytes.
+ *
+ * quant_mxfp8: x bf16 [R, K] -> q E4M3 [R, K] and sf_blocked uint8
+ *   [ceil(R / 128), K / 128, 512].  Used for activations (rows = tokens) and
+ *   for load-time weight prep (rows = output channels).  K % 128 == 0. */
+fq_status quant_mxfp8(const uint16_t* x, int64_t R, int64_t K, uint8_t* q, uint8_t* sf_blocked, fq_stream_t stream);
+
+/* Y[m, n] = bf16( sum_k (qx[m,k] * 2^(sx[m,k/32]-127)) * (qw[n,k] * 2^(sw[n,k/32]-127)) ),
+ * accumulated in fp32 by the tensor cores (tcgen05 block-scaled MMA).
+ *   xq, xsf : activations [M, K] and their blocked scales (quant_mxfp8)
+ *   wq, wsf : weights [N, K] (K-major) and their blocked scales
+ *   y       : bf16 [M, N]
+ *   ws      : fq_workspace_bytes(FQ_OP_MXFP8_LINEAR, M, K, N, 0) bytes
+ * K % 128 == 0, N % 16 == 0.  Partial tiles are summed in a fixed order, so
+ * repeated calls give identical bits. */
+fq_status mxfp8_linear(const uint8_t* xq, const uint8_t* xsf, int64_t M, int64_t K, const uint8_t* wq,
+                       const uint8_t* wsf, int64_t N, uint16_t* y, void* ws, size_t ws_bytes, fq_stream_t stream);
 
 /* ------------------------------------------------------------------- MoE */
 

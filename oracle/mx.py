@@ -15,6 +15,13 @@ Blocks run along the last (K) dimension of a row-major [R, K] tensor, K a
 multiple of 32; scales are stored [R, K/32] as bytes.  The same rule makes
 both operands of the linear (activations per token, weights per output row).
 
+Scale storage read by the linear (the consumer's native layout, as [PR]
+has the producer write its consumer's layout): for every 128 rows and every
+128-element K block, one 512-byte chunk; byte
+    (r % 32) * 16 + ((r % 128) // 32) * 4 + (k // 32) % 4
+of chunk (r // 128, k // 128) holds row r's scale for K block k // 32.  Rows
+past R in the last chunk row are zero bytes.
+
 Linear: Y[m, n] = bf16_RN( sum_b 2^(ex[m,b] + ew[n,b]) * sum_{k in b} qx[m,k] qw[n,k] ),
 the exact value rounded once (the GPU accumulates in fp32 inside the tensor
 core and is held to 1e-2 relative + 1e-3 absolute).
@@ -85,3 +92,28 @@ def _is_bf16_tie(v):
     b = np.asarray([v], np.float64).view(np.uint64)[0]
     mant = int(b) & ((1 << 52) - 1)
     return (mant & ((1 << 45) - 1)) == (1 << 44)
+
+
+def pack_sf_blocked(sf):
+    """UE8M0 bytes [R, K/32] -> blocked storage uint8 [ceil(R/128), K/128, 512]."""
+    sf = np.asarray(sf, np.uint8)
+    R, NB = sf.shape
+    if NB % 4:
+        raise ValueError("K must be a multiple of 128")
+    RB = (R + 127) // 128
+    out = np.zeros((RB, NB // 4, 512), np.uint8)
+    for r in range(R):
+        for b in range(NB):
+            out[r // 128, b // 4, (r % 32) * 16 + ((r % 128) // 32) * 4 + b % 4] = sf[r, b]
+    return out
+
+
+def unpack_sf_blocked(blocked, R):
+    """Inverse of pack_sf_blocked."""
+    blocked = np.asarray(blocked, np.uint8)
+    RB, KB, _ = blocked.shape
+    sf = np.zeros((R, KB * 4), np.uint8)
+    for r in range(R):
+        for b in range(KB * 4):
+            sf[r, b] = blocked[r // 128, b // 4, (r % 32) * 16 + ((r % 128) // 32) * 4 + b % 4]
+    return sf

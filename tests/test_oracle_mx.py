@@ -90,3 +90,17 @@ def test_linear_integer_case_and_scale_doubling():
     # +1 on every activation scale byte doubles Y exactly
     y2 = mx.mxfp8_linear(qx, sx + 1, qw, sw)
     assert np.array_equal(codecs.bf16_to_f32(y2), 2 * codecs.bf16_to_f32(y))
+
+
+def test_blocked_scale_layout_by_hand():
+    # R = 130 rows, K = 256: chunks [2, 2, 512]; row 33, K block 5 -> chunk (0, 1),
+    # byte (33 % 32) * 16 + (33 // 32) * 4 + 5 % 4 = 16 + 4 + 1 = 21; row 129, block 2 ->
+    # chunk (1, 0), byte 1 * 16 + 0 + 2 = 18
+    sf = np.zeros((130, 8), np.uint8)
+    sf[33, 5] = 200
+    sf[129, 2] = 17
+    b = mx.pack_sf_blocked(sf)
+    assert b.shape == (2, 2, 512)
+    assert b[0, 1, 21] == 200 and b[1, 0, 18] == 17
+    assert int(b.astype(np.int64).sum()) == 217          # everything else zero, incl. rows 130..255
+    assert np.array_equal(mx.unpack_sf_blocked(b, 130), sf)
