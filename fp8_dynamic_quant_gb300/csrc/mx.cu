@@ -305,19 +305,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 16; ++j) acc[j] = ok ? __uint_as_float(v[j]) : 0.0f;
             } else {
-              // every contributor's slot, this CTA's own included, in ascending CTA order
+              // every contributor's slot, this CTA's own included, added in
+              // ascending CTA order; four contributors' loads are in flight at once
 #pragma unroll
               for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-              for (int cc = c0; cc <= c1; ++cc) {
-                if (rb[cc + 1] == rb[cc]) continue;
-                const int first_tile = rb[cc] / KB;
-                const float* sl = p.slots + (2 * int64_t(cc) + (first_tile == tile ? 0 : 1)) * C::SLOT + nl +
-                                  16 * h * 128;
-                float v[16];
+              for (int cb = c0; cb <= c1; cb += 4) {
+                float v[4][16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = __ldcg(sl + j * 128);
+                for (int u = 0; u < 4; ++u) {
+                  const int cc = cb + u;
+                  const bool use = cc <= c1 && rb[cc + 1] != rb[cc];
+                  const int first_tile = use ? rb[cc] / KB : tile;
+                  const float* sl = p.slots + (2 * int64_t(use ? cc : b) + (first_tile == tile ? 0 : 1)) * C::SLOT +
+                                    nl + 16 * h * 128;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[j] = __fadd_rn(acc[j], v[j]);
+                  for (int j = 0; j < 16; ++j) v[u][j] = use ? __ldcg(sl + j * 128) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (cb + u <= c1 && rb[cb + u + 1] != rb[cb + u]) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] = __fadd_rn(acc[j], v[u][j]);
+                  }
               }
             }
 #pragma unroll
@@ -428,7 +437,10 @@ extern "C" __attribute__((visibility("default"))) fq_status mxfp8_linear(const u
   if (!tensor_map_u8_2d(&tw_map, wq, uint64_t(K), uint64_t(N), uint64_t(K), mxk::kBK, 128u) ||
       !tensor_map_u8_2d(&tx_map, xq, uint64_t(K), uint64_t(M), uint64_t(K), mxk::kBK, uint32_t(mt)))
     return FQ_ERR_CUDA;
-  const int grid = int(p.total < d.sm_count ? p.total : d.sm_count);
+  // at least 4 k-blocks per CTA: a CTA's fixed cost (pipeline fill, epilogue)
+  // and a tile's stream-K hand-off grow with the number of CTAs sharing it
+  const int64_t by_work = (p.total + 3) / 4;
+  const int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
   const bool pdl = pdl_enabled();
   cudaError_t e;
   switch (mt) {
