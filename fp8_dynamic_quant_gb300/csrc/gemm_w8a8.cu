@@ -1337,9 +1337,10 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   const int64_t tiles224 = ((N + 223) / 224) * m_tiles;
   bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
   // Few tiles (small N): 32-row tiles, each split over K by a cluster of 4 CTAs
-  // with a distributed-shared-memory reduction, when that fills >= 1/2 the GPU.
+  // with a distributed-shared-memory reduction, when that fills >= 1/2 the GPU
+  // (token tiles up to 32; at 64 the tcgen05 kernel measured faster).
   const int64_t ctas_cl = ((N + 31) / 32) * m_tiles * 4;
-  bool cluster = !data_parallel && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
+  bool cluster = !data_parallel && mt <= 32 && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
   const int force = forced_schedule();
   if (force == SCHED_DP && mt <= 16 && tiles224 <= kMaxGrid) {
     data_parallel = true;
@@ -1414,7 +1415,11 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     return FQ_ERR_CUDA;
   const CUtensorMap* tw = &tw_map;
   const CUtensorMap* tx = &tx_map;
-  const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
+  // tcgen05 path: at least 4 k-blocks per CTA (its fixed cost - tensor-memory
+  // set-up, pipeline fill, epilogue - and a tile's hand-off grow with the CTAs
+  // sharing the tile)
+  const int64_t work = umma ? (p.total + 3) / 4 : p.total;
+  const int grid = data_parallel ? int(tiles) : int(work < d.sm_count ? (work > 0 ? work : 1) : d.sm_count);
   debug_schedule("w8a8_linear", M, K, N, mt_run, data_parallel ? "dp224" : (umma ? "umma" : "streamk"), grid);
   const bool pdl = pdl_enabled();
   cudaError_t e;
