@@ -799,7 +799,8 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
 
 template <int MT, bool GROUPED>
 __global__ void __launch_bounds__(um::kThreads, 1)
-    w8a8_umma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
+    w8a8_umma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                     const __grid_constant__ CUtensorMap tmX16, const __grid_constant__ CUtensorMap tmX32, Problem p) {
   using C = um::Cfg<MT>;
   constexpr int SR = C::RAW_STAGES, SO = C::OP_STAGES, XT = MT / 32, CH = C::CH;
   constexpr int kThreads = um::kThreads, kConv = um::kConvWarps * 32, kEpi = um::kEpiWarps * 32;
@@ -847,6 +848,8 @@ __global__ void __launch_bounds__(um::kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmX16);
+    tma_prefetch_desc(&tmX32);
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem, um::kTmemCols);
@@ -905,11 +908,20 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const int npre = n_it < SR ? n_it : SR;
+      // activation box: only as many token rows as the tile holds (16, 32 or
+      // MT); rows past them in the stage are stale and feed output columns
+      // that are never stored
+      auto xrows = [&](int rows) { return rows <= 16 ? 16 : (rows <= 32 ? 32 : MT); };
+      auto load_x = [&](int s_, int kb_, const TileCoord& t_) {
+        const int xr = xrows(t_.rows);
+        const CUtensorMap* m = xr == 16 ? &tmX16 : (xr == 32 ? &tmX32 : &tmX);
+        tma_load_2d(raw + s_ * C::RAW + C::W_BYTES, m, &raw_full[s_], kb_ * kBK, t_.x_row, pol_x);
+      };
       {  // weights do not depend on the previous kernel: issue them first
         int tile = begin / KB, kb = begin - tile * KB;
         TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s);
         for (int r = 0; r < npre; ++r) {
-          mbar_arrive_expect_tx(&raw_full[r], C::RAW);
+          mbar_arrive_expect_tx(&raw_full[r], uint32_t(C::W_BYTES + xrows(tc.rows) * kBK));
           tma_load_2d(raw + r * C::RAW, &tmW, &raw_full[r], kb * kBK, tc.w_row, pol_w);
           if (++kb == KB && r + 1 < npre) {
             kb = 0;
@@ -924,16 +936,16 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       for (int r = 0; r < n_it; ++r) {
         const int s = r % SR;
         if (r < npre) {
-          tma_load_2d(raw + s * C::RAW + C::W_BYTES, &tmX, &raw_full[s], kb * kBK, tc.x_row, pol_x);
+          load_x(s, kb, tc);
         } else {
           if (s_abort || !mbar_wait(&raw_empty[s], uint32_t((r / SR - 1) & 1))) {
             if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
             s_abort = 1;
             break;
           }
-          mbar_arrive_expect_tx(&raw_full[s], C::RAW);
+          mbar_arrive_expect_tx(&raw_full[s], uint32_t(C::W_BYTES + xrows(tc.rows) * kBK));
           tma_load_2d(raw + s * C::RAW, &tmW, &raw_full[s], kb * kBK, tc.w_row, pol_w);
-          tma_load_2d(raw + s * C::RAW + C::W_BYTES, &tmX, &raw_full[s], kb * kBK, tc.x_row, pol_x);
+          load_x(s, kb, tc);
         }
         ++issued;
         if (++kb == KB && r + 1 < n_it) {
@@ -1271,8 +1283,8 @@ static cudaError_t launch_gemm(const CUtensorMap* tw, const CUtensorMap* tx, con
 }
 
 template <int MT, bool GROUPED>
-static cudaError_t launch_umma_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
-                                    cudaStream_t s, bool pdl) {
+static cudaError_t launch_umma_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const CUtensorMap* tx16,
+                                    const CUtensorMap* tx32, const Problem& p, int grid, cudaStream_t s, bool pdl) {
   using C = um::Cfg<MT>;
   auto k = w8a8_umma_kernel<MT, GROUPED>;
   static uint64_t attr_done = 0;  // one bit per device id
@@ -1283,7 +1295,7 @@ static cudaError_t launch_umma_gemm(const CUtensorMap* tw, const CUtensorMap* tx
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << (dev & 63);
   }
-  return launch(k, dim3(grid), dim3(um::kThreads), size_t(C::SMEM), s, pdl, *tw, *tx, p);
+  return launch(k, dim3(grid), dim3(um::kThreads), size_t(C::SMEM), s, pdl, *tw, *tx, *tx16, *tx32, p);
 }
 
 template <int MT>
@@ -1424,8 +1436,12 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   const bool pdl = pdl_enabled();
   cudaError_t e;
   if (umma) {
-    e = mt_run == 32 ? launch_umma_gemm<32, false>(tw, tx, p, grid, s, pdl)
-                     : launch_umma_gemm<64, false>(tw, tx, p, grid, s, pdl);
+    CUtensorMap tx16, tx32;  // smaller activation boxes for tiles with few token rows
+    if (!tensor_map_u8_2d(&tx16, xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, 16u) ||
+        !tensor_map_u8_2d(&tx32, xq, uint64_t(K), uint64_t(M), uint64_t(K), kBK, 32u))
+      return FQ_ERR_CUDA;
+    e = mt_run == 32 ? launch_umma_gemm<32, false>(tw, tx, &tx16, &tx32, p, grid, s, pdl)
+                     : launch_umma_gemm<64, false>(tw, tx, &tx16, &tx32, p, grid, s, pdl);
   } else if (data_parallel) {
     e = mt == 8 ? launch_gemm<8, 14, false>(tw, tx, p, grid, s, pdl) : launch_gemm<16, 14, false>(tw, tx, p, grid, s, pdl);
   } else {
@@ -1546,7 +1562,11 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(
   const bool umma = forced_schedule() != SCHED_STREAMK;
   debug_schedule("w8a8_grouped_linear", R, K, N, mt, umma ? "umma" : "streamk", d.sm_count);
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return cuda_status(umma ? launch_umma_gemm<mt, true>(tw, tx, p, d.sm_count, s, pdl_enabled())
+  CUtensorMap tx16, tx32;
+  if (umma && (!tensor_map_u8_2d(&tx16, xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, 16u) ||
+               !tensor_map_u8_2d(&tx32, xq, uint64_t(K), uint64_t(R), uint64_t(K), kBK, 32u)))
+    return FQ_ERR_CUDA;
+  return cuda_status(umma ? launch_umma_gemm<mt, true>(tw, tx, &tx16, &tx32, p, d.sm_count, s, pdl_enabled())
                           : launch_gemm<mt, 8, true>(tw, tx, p, d.sm_count, s, pdl_enabled()));
 }
 
