@@ -196,7 +196,13 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
   __shared__ int rb[kMaxGrid + 1];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const bool producer = warp == kCW && lane == 0;
+  // The producer thread sets up the ring and, for dense problems, issues the
+  // first stages of weights before anything else: they depend on nothing, and
+  // at decode sizes every cycle before the first copy adds to the kernel time.
+  int pre = 0;  // weight stages already issued (producer thread)
+  if (producer) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kCW);
@@ -205,10 +211,24 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     s_issued = 0;
     s_consumed = 0;
     s_abort = 0;
-  }
-  if (warp == kCW && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    if (!GROUPED) {
+      // this CTA's stream-K range, as rb[] below tabulates it
+      const int b0 = int(int64_t(b) * p.total / G), b1 = int(int64_t(b + 1) * p.total / G);
+      pre = min(b1 - b0, S);
+      const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+      int tile = b0 / p.KB, kb = b0 - tile * p.KB;
+      TileCoord tc = decode_tile<MT, BN, GROUPED>(p, tile, nullptr);
+      for (int r = 0; r < pre; ++r) {
+        mbar_arrive_expect_tx(&full[r], C::STAGE);
+        tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], kb * kBK, tc.w_row, pol_w);
+        if (++kb == p.KB && r + 1 < pre) {
+          kb = 0;
+          tc = decode_tile<MT, BN, GROUPED>(p, ++tile, nullptr);
+        }
+      }
+    }
   }
 
   int64_t I = p.total;
@@ -250,7 +270,6 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
   }
   __syncthreads();
 
-  const int G = gridDim.x, b = blockIdx.x;
   for (int c = tid; c <= G; c += kThreads) rb[c] = int(int64_t(c) * I / G);
   __syncthreads();
   const int begin = rb[b], end = rb[b + 1];
@@ -266,7 +285,8 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
       const int n_it = end - begin;
       const int npre = n_it < S ? n_it : S;
       // weights do not depend on the previous kernel: issue them first
-      {
+      // (dense problems issued them at kernel entry)
+      if (GROUPED) {
         int tile = begin / KB, kb = begin - tile * KB;
         TileCoord tc = decode_tile<MT, BN, GROUPED>(p, tile, tile_start_s);
         for (int r = 0; r < npre; ++r) {
@@ -517,30 +537,37 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
 // cluster of CL CTAs shares one tile of BN = 8 * CL weight rows and splits K.
 // Each CTA accumulates its K-range exactly (int32), then the partials are
 // reduce-scattered through distributed shared memory: CTA q of the cluster
-// owns rows [8q, 8q + 8) of the tile, receives the CL partial slices of those
+// owns rows [8q, 8q + 8) of the tile, receives the partial slices of those
 // rows, sums them, dequantizes and writes 16-byte rows of y.  No global
 // partial sums, counters or second pass.
-template <int MT, int CW, int CL>
+// Inside a CTA, KS consumer warps share each 16-row block and split every
+// k-block's eight k16 steps among themselves: with one block of rows per
+// warp the steps of a k-block form one dependent chain per warp and the
+// few warps of a CTA leave the schedulers idle.  Each k-split warp sends
+// its own partial slice, so the owner sums CL * KS slices.
+template <int MT, int RB, int CL, int KS>
 struct CCfg {
   static constexpr int NT = MT / 8;
-  static constexpr int BN = 16 * CW;
+  static constexpr int BN = 16 * RB;               // RB blocks of 16 weight rows
+  static constexpr int CW = RB * KS;               // consumer warps
   static constexpr int THREADS = (CW + 1) * 32;
   static constexpr int W_BYTES = BN * kBK;
   static constexpr int X_BYTES = MT * kBK;
   static constexpr int STAGE = W_BYTES + X_BYTES;
-  static constexpr int RECV = CL * 8 * MT * 4;  // [CL ranks][8 rows][MT tokens] int32
+  static constexpr int RECV = CL * KS * 8 * MT * 4;  // [CL ranks][KS k-splits][8 rows][MT tokens] int32
   static constexpr int STAGES_FIT = (212 * 1024 - RECV - 2048) / STAGE;
   static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
   static constexpr int SMEM = STAGES * STAGE + RECV + 2 * STAGES * 8 + 64 + 1024;
   static_assert(BN == 8 * CL, "each cluster rank owns 8 rows");
+  static_assert(KS == 1 || KS == 2 || KS == 4, "k16 steps of a k-block per warp: 8, 4 or 2");
   static_assert(STAGES >= 2, "pipeline too shallow");
 };
 
-template <int MT, int CW, int CL>
-__global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
+template <int MT, int RB, int CL, int KS>
+__global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, 1)
     w8a8_cluster_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
-  using C = CCfg<MT, CW, CL>;
-  constexpr int NT = C::NT, S = C::STAGES, BN = C::BN, kCW = CW;
+  using C = CCfg<MT, RB, CL, KS>;
+  constexpr int NT = C::NT, S = C::STAGES, BN = C::BN, kCW = C::CW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -553,7 +580,15 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = int(cluster_ctarank());
   const int tile = blockIdx.x / CL;
-  if (tid == 0) {
+  const int KB = p.KB;
+  const int kb0 = rank * KB / CL, kb1 = (rank + 1) * KB / CL;
+  const int n_it = kb1 - kb0;
+  const int npre = n_it < S ? n_it : S;
+  const TileCoord tc = decode_tile<MT, BN, false>(p, tile, nullptr);
+  // The producer thread sets up the ring and issues the first stages of
+  // weights before anything else: they depend on nothing, and at decode sizes
+  // every cycle before the first copy adds to the kernel time.
+  if (warp == kCW && lane == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kCW);
@@ -562,21 +597,20 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
     s_issued = 0;
     s_consumed = 0;
     s_abort = 0;
-  }
-  if (warp == kCW && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+    for (int r = 0; r < npre; ++r) {
+      mbar_arrive_expect_tx(&full[r], C::STAGE);
+      tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], (kb0 + r) * kBK, tc.w_row, pol_w);
+    }
   }
+  // the ring is initialised before any thread waits on it
+  __syncthreads();
   // Every CTA of the cluster must be running before any distributed-smem
   // write: arrive now, wait just before the scatter (keeps it off the
   // critical path of the weight stream).
-  __syncwarp();
   cluster_arrive_relaxed();
-
-  const int KB = p.KB;
-  const int kb0 = rank * KB / CL, kb1 = (rank + 1) * KB / CL;
-  const int n_it = kb1 - kb0;
-  const TileCoord tc = decode_tile<MT, BN, false>(p, tile, nullptr);
   // epilogue scales of the rows this CTA owns (8 channels, one token per thread)
   const int n_first = tc.n0 + 8 * rank;
   float sw_own[8];
@@ -588,11 +622,6 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
     if (lane == 0 && n_it > 0) {
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const int npre = n_it < S ? n_it : S;
-      for (int r = 0; r < npre; ++r) {
-        mbar_arrive_expect_tx(&full[r], C::STAGE);
-        tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], (kb0 + r) * kBK, tc.w_row, pol_w);
-      }
       pdl_wait();
       int issued = 0;
       for (int r = 0; r < n_it; ++r) {
@@ -620,6 +649,13 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
     pdl_launch_dependents();
     const int g = lane >> 2, c = lane & 3;
     const int rg = frag_row(g);
+    // warp -> (16-row block rbk, k-split kq): kq takes 16-byte chunk half
+    // HQ of every k-block row (KS >= 2) and, with KS = 4, two of its four words
+    const int rbk = warp % RB, kq = warp / RB;
+    constexpr int NH = KS == 1 ? 2 : 1;   // 64-byte halves of a k-block per warp
+    constexpr int NW = KS == 4 ? 2 : 4;   // k16 steps per half
+    const int h0 = KS == 1 ? 0 : (KS == 2 ? kq : kq >> 1);
+    const bool hi_words = KS == 4 && (kq & 1);
     constexpr int NACC = NT <= 2 ? 2 : 1;
     float accf[NACC][NT][4];
     int acci[NT][4];
@@ -632,9 +668,21 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
         acci[j][r] = 0;
       }
     const uint32_t sbase = smem_u32(stages);
-    const uint32_t rowW0 = uint32_t((16 * warp + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
+    const uint32_t rowW0 = uint32_t((16 * rbk + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
     const int rows_cur = tc.rows;
     int nk = 0, consumed = 0;
+    // the four words of a 16-byte chunk, or the two this warp takes
+    auto pick = [&](const uint4& v, uint32_t (&w)[NW]) {
+      if constexpr (NW == 4) {
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+      } else {
+        w[0] = hi_words ? v.z : v.x;
+        w[1] = hi_words ? v.w : v.y;
+      }
+    };
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
       bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
@@ -644,24 +692,25 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
       }
       const uint32_t st = sbase + uint32_t(s * C::STAGE);
 #pragma unroll
-      for (int h = 0; h < 2 && ok; ++h) {
+      for (int hh = 0; hh < NH && ok; ++hh) {
+        const int h = h0 + hh;
         const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
-        const uint4 wa = lds128(st + rowW0 + q);
-        const uint4 wb = lds128(st + rowW1 + q);
-        uint4 xv[NT];
+        uint32_t wa[NW], wb[NW], wx[NT][NW];
+        pick(lds128(st + rowW0 + q), wa);
+        pick(lds128(st + rowW1 + q), wb);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) xv[j] = lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q);
+        for (int j = 0; j < NT; ++j) pick(lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q), wx[j]);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
+        for (int ks = 0; ks < NW; ++ks) {
           uint32_t a0, a1, a2, a3;
-          i8x4_to_f16(word_of(wa, ks), a0, a2);
-          i8x4_to_f16(word_of(wb, ks), a1, a3);
+          i8x4_to_f16(wa[ks], a0, a2);
+          i8x4_to_f16(wb[ks], a1, a3);
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
             if (8 * j < rows_cur) {
               uint32_t b0, b1;
-              i8x4_to_f16(word_of(xv[j], ks), b0, b1);
-              mma_f16(accf[h % NACC][j], a0, a1, a2, a3, b0, b1);
+              i8x4_to_f16(wx[j][ks], b0, b1);
+              mma_f16(accf[(NH == 2 ? hh : ks) % NACC][j], a0, a1, a2, a3, b0, b1);
             }
           }
         }
@@ -687,16 +736,17 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
       }
     }
     if (tid < MT && tid < tc.rows) sx_own = __ldg(p.sx + tc.x_row + tid);
-    // reduce-scatter: row 16*warp + R(g) (+8) belongs to cluster rank 2*warp (+1)
+    // reduce-scatter: row 16*rbk + R(g) (+8) belongs to cluster rank 2*rbk (+1);
+    // each (rank, k-split) pair has its own slice at the owner
     cluster_wait_acquire();  // all CTAs of the cluster have started
     const uint32_t recv_base = smem_u32(recv);
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
-        const int owner = 2 * warp + (rr >> 1);
+        const int owner = 2 * rbk + (rr >> 1);
         const int ml = 8 * j + frag_row(2 * c + (rr & 1));
-        const uint32_t off = uint32_t(((rank * 8 + rg) * MT + ml) * 4);
+        const uint32_t off = uint32_t((((rank * KS + kq) * 8 + rg) * MT + ml) * 4);
         st_cluster_u32(mapa_shared(recv_base + off, uint32_t(owner)), uint32_t(acci[j][rr]));
       }
     if (tid == 0) s_consumed = consumed;
@@ -714,7 +764,7 @@ __global__ void __launch_bounds__(CCfg<MT, CW, CL>::THREADS, 1)
         for (int r2 = 0; r2 < 8; r2 += 2) {
           int a0 = 0, a1 = 0;
 #pragma unroll
-          for (int rk = 0; rk < CL; ++rk) {
+          for (int rk = 0; rk < CL * KS; ++rk) {
             a0 += recv[(rk * 8 + r2) * MT + ml];
             a1 += recv[(rk * 8 + r2 + 1) * MT + ml];
           }
@@ -791,6 +841,12 @@ struct Cfg {
   static_assert(RAW_STAGES >= 3, "pipeline too shallow");
   static_assert(MT == 32 || MT == 64, "token tile");
 };
+
+// Activation box height: only as many token rows as the tile holds (16, 32
+// or MT); rows past them in the stage are stale and feed output columns that
+// are never stored.
+template <int MT>
+__device__ __forceinline__ int x_box_rows(int rows) { return rows <= 16 ? 16 : (rows <= 32 ? 32 : MT); }
 }  // namespace um
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -844,12 +900,30 @@ __global__ void __launch_bounds__(um::kThreads, 1)
     s_issued = 0;
     s_consumed = 0;
     s_abort = 0;
-  }
-  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmX16);
     tma_prefetch_desc(&tmX32);
+    // Thread 0 is the producer.  Dense problems issue their first weight
+    // stages right here: they depend on nothing, and at decode sizes every
+    // cycle before the first copy adds to the kernel time.
+    if (!GROUPED) {
+      // this CTA's stream-K range, as rb[] below tabulates it
+      const int b0 = int(int64_t(blockIdx.x) * p.total / gridDim.x);
+      const int b1 = int(int64_t(blockIdx.x + 1) * p.total / gridDim.x);
+      const int pre = min(b1 - b0, SR);
+      const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+      int tile = b0 / p.KB, kb = b0 - tile * p.KB;
+      TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, nullptr);
+      for (int r = 0; r < pre; ++r) {
+        mbar_arrive_expect_tx(&raw_full[r], uint32_t(C::W_BYTES + um::x_box_rows<MT>(tc.rows) * kBK));
+        tma_load_2d(raw + r * C::RAW, &tmW, &raw_full[r], kb * kBK, tc.w_row, pol_w);
+        if (++kb == p.KB && r + 1 < pre) {
+          kb = 0;
+          tc = decode_tile<MT, 128, GROUPED>(p, ++tile, nullptr);
+        }
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem, um::kTmemCols);
@@ -908,16 +982,13 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const int npre = n_it < SR ? n_it : SR;
-      // activation box: only as many token rows as the tile holds (16, 32 or
-      // MT); rows past them in the stage are stale and feed output columns
-      // that are never stored
-      auto xrows = [&](int rows) { return rows <= 16 ? 16 : (rows <= 32 ? 32 : MT); };
+      auto xrows = [&](int rows) { return um::x_box_rows<MT>(rows); };
       auto load_x = [&](int s_, int kb_, const TileCoord& t_) {
         const int xr = xrows(t_.rows);
         const CUtensorMap* m = xr == 16 ? &tmX16 : (xr == 32 ? &tmX32 : &tmX);
         tma_load_2d(raw + s_ * C::RAW + C::W_BYTES, m, &raw_full[s_], kb_ * kBK, t_.x_row, pol_x);
       };
-      {  // weights do not depend on the previous kernel: issue them first
+      if (GROUPED) {  // weights do not depend on the previous kernel: issue them first (dense: done above)
         int tile = begin / KB, kb = begin - tile * KB;
         TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s);
         for (int r = 0; r < npre; ++r) {
@@ -1301,8 +1372,8 @@ static cudaError_t launch_umma_gemm(const CUtensorMap* tw, const CUtensorMap* tx
 template <int MT>
 static cudaError_t launch_cluster_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
                                        cudaStream_t s, bool pdl) {
-  using C = CCfg<MT, 2, 4>;
-  auto k = w8a8_cluster_kernel<MT, 2, 4>;
+  using C = CCfg<MT, 2, 4, 4>;
+  auto k = w8a8_cluster_kernel<MT, 2, 4, 4>;
   static uint64_t attr_done = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1350,9 +1421,9 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
   // Few tiles (small N): 32-row tiles, each split over K by a cluster of 4 CTAs
   // with a distributed-shared-memory reduction, when that fills >= 1/2 the GPU
-  // (token tiles up to 32; at 64 the tcgen05 kernel measured faster).
+  // (every token tile: with its k-split warps it beats the tcgen05 kernel at 64).
   const int64_t ctas_cl = ((N + 31) / 32) * m_tiles * 4;
-  bool cluster = !data_parallel && mt <= 32 && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
+  bool cluster = !data_parallel && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
   const int force = forced_schedule();
   if (force == SCHED_DP && mt <= 16 && tiles224 <= kMaxGrid) {
     data_parallel = true;
