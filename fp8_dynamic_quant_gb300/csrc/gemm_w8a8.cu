@@ -50,23 +50,25 @@ constexpr int kFlushBlocks = 8;      // fold fp32 -> int32 every 8 k-blocks (102
 constexpr int kBN = 128;             // weight rows per tile in the stream-K configuration (8 consumer warps)
 
 // MT tokens per tile, CW consumer warps of 16 weight rows each (BN = 16 * CW
-// rows per tile), plus one producer warp.
+// rows per tile), one producer warp and one activation-converter warp.
 template <int MT, int CW>
 struct Cfg {
   static constexpr int NT = MT / 8;
   static constexpr int BN = 16 * CW;
-  static constexpr int THREADS = (CW + 1) * 32;
+  static constexpr int THREADS = (CW + 2) * 32;
   static constexpr int W_BYTES = BN * kBK;
   static constexpr int X_BYTES = MT * kBK;
   static constexpr int STAGE = W_BYTES + X_BYTES;           // multiple of 1024
+  static constexpr int XF = MT * kBK * 2;                   // f16 activation fragments of a stage
   static constexpr int EPI = BN * MT * 2;                   // bf16 staging
   // Loaded HBM latency is several microseconds, so each SM needs ~200 KB of
-  // weights in flight to stream at full rate: fill the shared-memory budget.
-  static constexpr int SMEM_BUDGET = 212 * 1024;
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - EPI - 2048) / STAGE;
+  // weights in flight to stream at full rate: fill the shared-memory budget
+  // (the largest configuration still leaves room for the static tables).
+  static constexpr int SMEM_BUDGET = 223 * 1024;
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - EPI - 2048) / (STAGE + XF);
   static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
   static constexpr int SLOT = BN * MT;                      // int32 per slot
-  static constexpr int SMEM = STAGES * STAGE + EPI + 2 * STAGES * 8 + 64 + 1024;  // + alignment slack
+  static constexpr int SMEM = STAGES * (STAGE + XF) + EPI + 3 * STAGES * 8 + 64 + 1024;  // + alignment slack
   static_assert(STAGES >= 3, "pipeline too shallow");
 };
 
@@ -98,6 +100,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // int8 x4 -> two f16x2: lo = (b0, b1), hi = (b2, b3), exactly.
@@ -186,9 +192,11 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + S * C::STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE + C::EPI);
+  uint8_t* xfrag = smem + S * C::STAGE;  // [S][h][NT][2][32 lanes] x 16 bytes of f16 B fragments
+  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + S * (C::STAGE + C::XF));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * (C::STAGE + C::XF) + C::EPI);
   uint64_t* empty = full + S;
+  uint64_t* xready = empty + S;
   __shared__ int s_flag;
   __shared__ int s_issued, s_consumed;
   __shared__ volatile int s_abort;  // set after any timed-out wait: later waits are skipped
@@ -198,6 +206,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, b = blockIdx.x;
   const bool producer = warp == kCW && lane == 0;
+  constexpr int kConv = CW + 1;  // the activation-converter warp
   // The producer thread sets up the ring and, for dense problems, issues the
   // first stages of weights before anything else: they depend on nothing, and
   // at decode sizes every cycle before the first copy adds to the kernel time.
@@ -206,6 +215,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kCW);
+      mbar_init(&xready[i], 1);
     }
     fence_barrier_init();
     s_issued = 0;
@@ -324,6 +334,46 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
       }
       s_issued = issued;
     }
+  } else if (warp == kConv) {
+    // ------------------------------------------------ activation converter
+    // Every consumer warp needs the same f16 B fragments of a stage's
+    // activation tile; converting them once here takes that integer work
+    // (a third of the consumers' at 8 tokens) off the fourteen consumer
+    // warps.  Lane l writes what consumer lane l reads: for each 64-byte half
+    // h and token group j, the f16 pairs of its 16-byte chunk, k16 steps 0-1
+    // then 2-3.
+    const int g = lane >> 2, c = lane & 3;
+    const int rg = frag_row(g);
+    const uint32_t sbase = smem_u32(stages), xbase = smem_u32(xfrag);
+    const int n_it = end - begin;
+    for (int r = 0; r < n_it; ++r) {
+      const int s = r % S;
+      if (s_abort || !mbar_wait(&full[s], uint32_t((r / S) & 1))) {
+        if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      const uint32_t st = sbase + uint32_t(s * C::STAGE) + uint32_t(C::W_BYTES);
+      const uint32_t xo = xbase + uint32_t(s * C::XF);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const uint4 v = lds128(st + uint32_t((8 * j + rg) * kBK) + q);
+          uint32_t f[8];
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) i8x4_to_f16(word_of(v, ks), f[2 * ks], f[2 * ks + 1]);
+          const uint32_t o = xo + uint32_t(((h * NT + j) * 2) * 512 + lane * 16);
+          sts128(o, f[0], f[1], f[2], f[3]);
+          sts128(o + 512, f[4], f[5], f[6], f[7]);
+        }
+      }
+      // generic-proxy reads of the stage before the async-proxy refill
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xready[s]);
+    }
   } else {
     // ------------------------------------------------ consumer warps
     pdl_wait();
@@ -347,7 +397,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
         for (int a = 0; a < NACC; ++a) accf[a][j][r] = 0.f;
         acci[j][r] = 0;
       }
-    const uint32_t sbase = smem_u32(stages);
+    const uint32_t sbase = smem_u32(stages), xbase = smem_u32(xfrag);
     const uint32_t rowW0 = uint32_t((16 * warp + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
     int tile = begin / KB, kb = begin - tile * KB;
     int seg_kb0 = kb;
@@ -380,34 +430,38 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     // named barriers - but skips waits and math, so every warp finishes.
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
-      bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
+      const uint32_t par = uint32_t((r / S) & 1);
+      bool ok = !s_abort && mbar_wait(&full[s], par) && mbar_wait(&xready[s], par);
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
       }
       const uint32_t st = sbase + uint32_t(s * C::STAGE);
+      const uint32_t xo = xbase + uint32_t(s * C::XF) + uint32_t(lane * 16);
 #pragma unroll
       for (int h = 0; h < 2 && ok; ++h) {
         const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
         const uint4 wa = lds128(st + rowW0 + q);
         const uint4 wb = lds128(st + rowW1 + q);
-        // 8-token groups past the tile's valid rows are skipped (uniform
-        // branch): an expert with 3 tokens in a 64-token tile costs one group
-        uint4 xv[NT];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) xv[j] = lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q);
+        for (int half = 0; half < 2; ++half) {
+          // B fragments of k16 steps 2*half and 2*half+1; 8-token groups past
+          // the tile's valid rows are skipped (uniform branch): an expert with
+          // 3 tokens in a 64-token tile costs one group
+          uint4 xv[NT];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          i8x4_to_f16(word_of(wa, ks), a0, a2);
-          i8x4_to_f16(word_of(wb, ks), a1, a3);
+          for (int j = 0; j < NT; ++j)
+            if (8 * j < rows_cur) xv[j] = lds128(xo + uint32_t(((h * NT + j) * 2 + half) * 512));
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            if (8 * j < rows_cur) {
-              uint32_t b0, b1;
-              i8x4_to_f16(word_of(xv[j], ks), b0, b1);
-              mma_f16(accf[h % NACC][j], a0, a1, a2, a3, b0, b1);
-            }
+          for (int kk = 0; kk < 2; ++kk) {
+            const int ks = 2 * half + kk;
+            uint32_t a0, a1, a2, a3;
+            i8x4_to_f16(word_of(wa, ks), a0, a2);
+            i8x4_to_f16(word_of(wb, ks), a1, a3);
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+              if (8 * j < rows_cur)
+                mma_f16(accf[h % NACC][j], a0, a1, a2, a3, word_of(xv[j], 2 * kk), word_of(xv[j], 2 * kk + 1));
           }
         }
       }
@@ -457,7 +511,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
           do_epi = s_flag != 0;
           if (do_epi) {
             // add the other contributors' partials; U slots in flight at once
-            constexpr int U = NT <= 2 ? 8 : (NT <= 4 ? 4 : 2);
+            constexpr int U = NT <= 2 ? 8 : (NT <= 4 ? 4 : 1);
             const int c0 = cta_of(rb, G, tile * KB), c1 = cta_of(rb, G, tile * KB + KB - 1);
             for (int cb = c0; cb <= c1; cb += U) {
               int32_t v[U][NT][4];
@@ -849,9 +903,6 @@ template <int MT>
 __device__ __forceinline__ int x_box_rows(int rows) { return rows <= 16 ? 16 : (rows <= 32 ? 32 : MT); }
 }  // namespace um
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 template <int MT, bool GROUPED>
 __global__ void __launch_bounds__(um::kThreads, 1)
