@@ -49,27 +49,34 @@ constexpr int kBK = 128;             // K bytes per k-block
 constexpr int kFlushBlocks = 8;      // fold fp32 -> int32 every 8 k-blocks (1024 K)
 constexpr int kBN = 128;             // weight rows per tile in the stream-K configuration (8 consumer warps)
 
+// Largest K whose whole quantized activation tile a CTA keeps in shared
+// memory when it quantizes the activations itself.
+constexpr int kFuseKMax = 1024;
+
 // MT tokens per tile, CW consumer warps of 16 weight rows each (BN = 16 * CW
-// rows per tile), one producer warp and one activation-converter warp.
-template <int MT, int CW>
+// rows per tile), one producer warp and one activation-converter warp.  FQ:
+// the CTA quantizes its activations itself (the stages then hold weights only).
+template <int MT, int CW, bool FQ = false>
 struct Cfg {
   static constexpr int NT = MT / 8;
   static constexpr int BN = 16 * CW;
   static constexpr int THREADS = (CW + 2) * 32;
   static constexpr int W_BYTES = BN * kBK;
   static constexpr int X_BYTES = MT * kBK;
-  static constexpr int STAGE = W_BYTES + X_BYTES;           // multiple of 1024
-  static constexpr int XF = MT * kBK * 2;                   // f16 activation fragments of a stage
-  static constexpr int EPI = BN * MT * 2;                   // bf16 staging
+  static constexpr int STAGE = W_BYTES + (FQ ? 0 : X_BYTES);  // multiple of 1024
+  static constexpr int XF = MT * kBK * 2;                     // f16 activation fragments of a stage
+  static constexpr int XQ = FQ ? MT * kFuseKMax : 0;          // quantized activation tile, all of K
+  static constexpr int EPI = BN * MT * 2;                     // bf16 staging
   // Loaded HBM latency is several microseconds, so each SM needs ~200 KB of
-  // weights in flight to stream at full rate: fill the shared-memory budget
-  // (the largest configuration still leaves room for the static tables).
-  static constexpr int SMEM_BUDGET = 223 * 1024;
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - EPI - 2048) / (STAGE + XF);
+  // weights in flight to stream at full rate: fill shared memory up to the
+  // opt-in maximum (232448 bytes) less the kernel's static tables.
+  static constexpr int SMEM_LIMIT = 232448 - 4160;
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - EPI - XQ - 1088) / (STAGE + XF + 24);
   static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
-  static constexpr int SLOT = BN * MT;                      // int32 per slot
-  static constexpr int SMEM = STAGES * (STAGE + XF) + EPI + 3 * STAGES * 8 + 64 + 1024;  // + alignment slack
+  static constexpr int SLOT = BN * MT;                        // int32 per slot
+  static constexpr int SMEM = STAGES * (STAGE + XF) + XQ + EPI + 3 * STAGES * 8 + 64 + 1024;  // + alignment slack
   static_assert(STAGES >= 3, "pipeline too shallow");
+  static_assert(SMEM <= SMEM_LIMIT, "shared-memory budget");
 };
 
 // Fragment row g (0..7) of a 16-row block reads shared-memory row R(g).  The
@@ -93,6 +100,9 @@ struct Problem {
   const int32_t* offsets;   // grouped: [E + 1]
   int E;                    // grouped: experts
   int w_reuse;              // weight tiles are read by more than one token tile
+  const uint16_t* x16;      // CTA-quantized activations: bf16 [M, K]
+  int8_t* xq_out;           // ... optional copy of the quantized activations [M, K]
+  float* sx_out;            // ... optional copy of their scales [M]
 };
 
 // ---------------------------------------------------------------- device helpers
@@ -184,19 +194,24 @@ __device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int MT, int CW, bool GROUPED>
-__global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
+template <int MT, int CW, bool GROUPED, bool FQ = false>
+__global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
     w8a8_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
-  using C = Cfg<MT, CW>;
+  using C = Cfg<MT, CW, FQ>;
+  static_assert(!(FQ && GROUPED), "CTA-quantized activations: dense problems only");
   constexpr int NT = C::NT, S = C::STAGES, BN = C::BN, kThreads = C::THREADS, kCW = CW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   uint8_t* xfrag = smem + S * C::STAGE;  // [S][h][NT][2][32 lanes] x 16 bytes of f16 B fragments
-  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + S * (C::STAGE + C::XF));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * (C::STAGE + C::XF) + C::EPI);
+  // FQ: the quantized activation tile, [k-block][MT rows][128 bytes], 16-byte
+  // chunks swizzled like the TMA's 128-byte mode (chunk ^ (row & 7))
+  uint8_t* xqs = smem + S * (C::STAGE + C::XF);
+  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + S * (C::STAGE + C::XF) + C::XQ);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * (C::STAGE + C::XF) + C::XQ + C::EPI);
   uint64_t* empty = full + S;
   uint64_t* xready = empty + S;
+  __shared__ float s_sxq[FQ ? MT : 1];
   __shared__ int s_flag;
   __shared__ int s_issued, s_consumed;
   __shared__ volatile int s_abort;  // set after any timed-out wait: later waits are skipped
@@ -315,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
       for (int r = 0; r < n_it; ++r) {
         const int s = r % S;
         if (r < npre) {
-          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
+          if (!FQ) tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
         } else {
           if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
             if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
@@ -324,7 +339,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
           }
           mbar_arrive_expect_tx(&full[s], C::STAGE);
           tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], kb * kBK, tc.w_row, pol_w);
-          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
+          if (!FQ) tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
         }
         ++issued;
         if (++kb == KB && r + 1 < n_it) {
@@ -344,8 +359,11 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     // then 2-3.
     const int g = lane >> 2, c = lane & 3;
     const int rg = frag_row(g);
-    const uint32_t sbase = smem_u32(stages), xbase = smem_u32(xfrag);
+    const uint32_t sbase = smem_u32(stages), xbase = smem_u32(xfrag), xqbase = smem_u32(xqs);
     const int n_it = end - begin;
+    // FQ: wait until the consumer warps have quantized the activation tile
+    if (FQ) named_bar_sync(2, (kCW + 1) * 32);
+    int kb = begin % KB;
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
       if (s_abort || !mbar_wait(&full[s], uint32_t((r / S) & 1))) {
@@ -353,7 +371,8 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
         s_abort = 1;
         break;
       }
-      const uint32_t st = sbase + uint32_t(s * C::STAGE) + uint32_t(C::W_BYTES);
+      const uint32_t st = FQ ? xqbase + uint32_t(kb * MT * kBK) : sbase + uint32_t(s * C::STAGE) + uint32_t(C::W_BYTES);
+      if (++kb == KB) kb = 0;
       const uint32_t xo = xbase + uint32_t(s * C::XF);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -381,6 +400,54 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
     // dependent may prefetch weights before its own wait, which is safe only
     // if every earlier kernel has finished.
     pdl_launch_dependents();
+    if constexpr (FQ) {
+      // Per-token quant of the whole activation tile (one tile per CTA, all of
+      // K), one row per warp, with the quant kernel's arithmetic: the warp's
+      // max is the row's absmax whatever the order, so the scale and codes
+      // are the quant kernel's bit for bit.  CTA 0 also writes the optional
+      // copies.  Meanwhile the first weight stages are still in flight.
+      const int rows = min(MT, p.M);
+      const int K8 = p.K / 8;
+      constexpr int VPL = kFuseKMax / 256;  // 16-byte vectors per lane
+      const uint32_t xqbase = smem_u32(xqs);
+      for (int m = warp; m < rows; m += kCW) {
+        const uint4* xr = reinterpret_cast<const uint4*>(p.x16) + int64_t(m) * K8;
+        uint4 v[VPL];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int idx = lane + 32 * i;
+          if (idx < K8) {
+            v[i] = ld_stream(xr + idx);
+            float f[8];
+            unpack8(v[i], f);
+            amax = fmaxf(amax, absmax8(f));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float sc = __fdiv_rn(amax, 127.0f);
+        const float inv = __frcp_rn(sc);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int idx = lane + 32 * i;
+          if (idx < K8) {
+            float f[8];
+            unpack8(v[i], f);
+            const uint2 qv = quant8_i8(f, sc, inv);
+            const int k = idx * 8;
+            const uint32_t a = xqbase + uint32_t(((k >> 7) * MT + m) * kBK + ((((k >> 4) & 7) ^ (m & 7)) << 4) + (k & 8));
+            asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(a), "r"(qv.x), "r"(qv.y) : "memory");
+            if (b == 0 && p.xq_out) *reinterpret_cast<uint2*>(p.xq_out + int64_t(m) * p.K + k) = qv;
+          }
+        }
+        if (lane == 0) {
+          s_sxq[m] = sc;
+          if (b == 0 && p.sx_out) p.sx_out[m] = sc;
+        }
+      }
+      named_bar_sync(2, (kCW + 1) * 32);  // with the converter warp
+    }
     const int g = lane >> 2, c = lane & 3;
     const int rg = frag_row(g);
     // With few token tiles, two fp32 chains (even / odd 64-byte halves of a
@@ -417,7 +484,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int ml = 8 * j + frag_row(2 * c + h);
-          sxr[j][h] = ml < tc.rows ? __ldg(p.sx + tc.x_row + ml) : 0.f;
+          sxr[j][h] = ml < tc.rows ? (FQ ? s_sxq[ml] : __ldg(p.sx + tc.x_row + ml)) : 0.f;
         }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -1388,11 +1455,11 @@ size_t ws_w8a8_grouped_linear(int64_t R, int64_t K, int64_t N, int64_t E) {
   return kCounterBytes + slots_bytes(d.sm_count, 64);
 }
 
-template <int MT, int CW, bool GROUPED>
+template <int MT, int CW, bool GROUPED, bool FQ = false>
 static cudaError_t launch_gemm(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid,
                                cudaStream_t s, bool pdl) {
-  using C = Cfg<MT, CW>;
-  auto k = w8a8_gemm_kernel<MT, CW, GROUPED>;
+  using C = Cfg<MT, CW, FQ>;
+  auto k = w8a8_gemm_kernel<MT, CW, GROUPED, FQ>;
   static uint64_t attr_done = 0;  // one bit per device id
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1458,6 +1525,22 @@ static void debug_schedule(const char* op, int64_t M, int64_t K, int64_t N, int 
 
 // Shared by the dense and fused entry points.  `counters` is the fixed
 // counter block at the head of the workspace; `slots` the partial-sum area.
+// The fused op runs as one launch when the dense schedule would stream one
+// whole 224-row tile per CTA and the whole quantized activation tile fits in
+// shared memory: each CTA quantizes the activations itself, one row per warp,
+// after the previous kernel has finished.  With 8-token tiles that beats a
+// separate quant launch; with 16 some warps take two rows one after the other
+// and the quant (measured) no longer hides under the first weight stages.
+static bool quant_in_gemm(int64_t M, int64_t K, int64_t N, const DevInfo& d) {
+  const int mt = pick_mt(M);
+  if (mt > 8 || M > mt || K > kFuseKMax) return false;
+  const int force = forced_schedule();
+  const int64_t tiles224 = (N + 223) / 224;
+  if (force == SCHED_DP) return tiles224 <= kMaxGrid;
+  if (force != SCHED_AUTO) return false;
+  return tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
+}
+
 fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K, const int8_t* w_nk, const float* sw,
                          int64_t N, uint16_t* y, uint32_t* counters, void* slots, size_t slots_avail, cudaStream_t s,
                          const DevInfo& d) {
@@ -1630,6 +1713,31 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
   // validate the GEMM part before launching the quant
   if (N > 0 && K > 0 && ws_bytes - kCounterBytes - xq_b - sx_b < slots_bytes(d.sm_count, slots_mt(M)))
     return FQ_ERR_WORKSPACE;
+  if (N > 0 && K > 0 && quant_in_gemm(M, K, N, d)) {
+    // one launch: every CTA quantizes the (small) activation tile itself
+    const int mt = pick_mt(M);
+    const int64_t tiles = (N + 223) / 224;
+    Problem p = {};
+    p.M = int(M);
+    p.N = int(N);
+    p.K = int(K);
+    p.KB = int((K + kBK - 1) / kBK);
+    p.m_tiles = 1;
+    p.n_tiles = int(tiles);
+    p.total = tiles * p.KB;
+    p.sw = sw;
+    p.y = y;
+    p.counters = reinterpret_cast<uint32_t*>(w8);
+    p.err = d.err_word;
+    p.x16 = x;
+    p.xq_out = xq_out;
+    p.sx_out = sx_out;
+    CUtensorMap tw_map;
+    if (!tensor_map_u8_2d(&tw_map, w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, 224u)) return FQ_ERR_CUDA;
+    debug_schedule("w8a8_quant_linear", M, K, N, mt, "dp224+quant", int(tiles));
+    const bool pdl = pdl_enabled();
+    return cuda_status(launch_gemm<8, 14, false, true>(&tw_map, &tw_map, p, int(tiles), s, pdl));
+  }
   if ((st = dynamic_quant_int8(x, M, K, xq, sx, stream)) != FQ_OK) return st;
   if (N == 0) return FQ_OK;
   if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(M) * size_t(N) * 2, s));

@@ -19,61 +19,6 @@
 
 namespace fq {
 
-// ---------------------------------------------------------------- shared math
-
-// q = clamp(rint(x / s), -127, 127) with x / s the IEEE fp32 quotient, ties
-// to even.  The quotient is first estimated as x * RN(1/s) (within 2.3e-5 of
-// the IEEE quotient for |x / s| <= 127); only when that estimate lies within
-// 2^-14 of a half-integer, where the two could round differently, is the
-// exact __fdiv_rn taken.  s == 0 only for an all-zero row (q = 0).  When
-// RN(1/s) is not finite (s below ~2.9e-39) every element takes the exact path.
-__device__ __forceinline__ int quant_i8(float x, float s, float inv_s) {
-  if (s == 0.0f) return 0;
-  const float y = __fmul_rn(x, inv_s);
-  float r = rintf(y);
-  const float d = fabsf(y - r);
-  if (!(fabsf(d - 0.5f) >= (1.0f / 16384.0f))) r = rintf(__fdiv_rn(x, s));  // also catches NaN from inf
-  r = fminf(fmaxf(r, -127.0f), 127.0f);
-  return static_cast<int>(r);
-}
-
-__device__ __forceinline__ uint32_t pack4_i8(int a, int b, int c, int d) {
-  return (uint32_t(a) & 0xFFu) | ((uint32_t(b) & 0xFFu) << 8) | ((uint32_t(c) & 0xFFu) << 16) |
-         ((uint32_t(d) & 0xFFu) << 24);
-}
-
-// 8 bf16 values in a uint4 -> floats.
-__device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ float absmax8(const float f[8]) {
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-  return m;
-}
-
-__device__ __forceinline__ uint2 quant8_i8(const float f[8], float s, float inv) {
-  uint2 o;
-  o.x = pack4_i8(quant_i8(f[0], s, inv), quant_i8(f[1], s, inv), quant_i8(f[2], s, inv), quant_i8(f[3], s, inv));
-  o.y = pack4_i8(quant_i8(f[4], s, inv), quant_i8(f[5], s, inv), quant_i8(f[6], s, inv), quant_i8(f[7], s, inv));
-  return o;
-}
-
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Block-wide max over blockDim.x threads (multiple of 32); `red` holds 32 floats.
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll

@@ -138,6 +138,60 @@ def test_fused_quant_linear_equals_two_steps(M, K, N):
     assert np.array_equal(bf16_to_np(y), want)
 
 
+# (M, K, N) where the dense schedule streams one whole 224-row tile per CTA
+# (114..148 tiles) with M <= 8 and K <= 1024: the fused op is one launch in
+# which every CTA quantizes the activations itself.  Ragged K (1008, 144, 16)
+# and N.
+FUSED_ONE_LAUNCH = [(1, 1024, 32768), (2, 1024, 32768), (3, 1024, 25600), (7, 1008, 30000), (8, 1024, 33152),
+                    (6, 512, 29008), (8, 1024, 32768), (5, 16, 26000), (4, 144, 33008)]
+
+
+def _fused_one_launch(x, w_nk, sw):
+    xd, w, s = bf16_to_dev(x), np_to_dev(w_nk), np_to_dev(sw)
+    y, xq, sx = fq.w8a8_quant_linear(xd, w, s, return_quant=True)
+    y_plain = fq.w8a8_quant_linear(xd, w, s)
+    torch.cuda.synchronize()
+    return bf16_to_np(y), bf16_to_np(y_plain), xq.cpu().numpy(), sx.cpu().numpy()
+
+
+@pytest.mark.parametrize("M,K,N", FUSED_ONE_LAUNCH)
+def test_fused_one_launch_bit_exact(M, K, N, monkeypatch, capfd):
+    """y, xq and sx of the one-launch fused op equal the oracle bit for bit (a zero row included)."""
+    monkeypatch.setenv("FQ_DEBUG_SCHEDULE", "1")
+    c = synth.int8_linear_case(M, K, N, 5000 + M + K + N)
+    x = c["x"].copy()
+    if M >= 3:
+        x[M - 1, :] = 0  # all-zero row: scale 0, codes 0
+    y, y_plain, q, s = _fused_one_launch(x, c["w_nk"], c["sw"])
+    assert "schedule=dp224+quant" in capfd.readouterr().err
+    want, oq, os_ = oi8.w8a8_quant_linear(x, c["w_nk"], c["sw"])
+    assert np.array_equal(q, oq) and np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(y, want), np.argwhere(y != want)[:5]
+    assert np.array_equal(y_plain, want)
+
+
+def test_fused_one_launch_forced_small_n_and_ties(monkeypatch, capfd):
+    """Forced data-parallel schedule on a small N, and rows whose quotients sit at k + 0.5."""
+    monkeypatch.setenv("FQ_DEBUG_SCHEDULE", "1")
+    monkeypatch.setenv("FQ_FORCE_SCHEDULE", "dp")
+    r = np.random.default_rng(11)
+    M, K, N = 8, 1024, 2240
+    amax = 127.0 * 1.5
+    rows = []
+    for m in range(M):
+        v = ((r.integers(-126, 126, K).astype(np.float64) + 0.5) * (amax / 127.0)).astype(np.float32)
+        v[m] = amax
+        rows.append(v)
+    x = codecs.f32_to_bf16(np.stack(rows))
+    w_nk = synth.int8_weights(N, K, 77)
+    sw = synth.channel_scales(N, 78)
+    y, y_plain, q, s = _fused_one_launch(x, w_nk, sw)
+    assert "schedule=dp224+quant" in capfd.readouterr().err
+    want, oq, os_ = oi8.w8a8_quant_linear(x, w_nk, sw)
+    assert np.array_equal(q, oq) and np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(y, want) and np.array_equal(y_plain, want)
+
+
 def test_workspace_counters_return_to_zero():
     c = synth.int8_linear_case(9, 4096, 1024, 11)
     q, s = oi8.dynamic_quant_int8(c["x"])
