@@ -408,6 +408,10 @@ size_t ws_w8a8_linear(int64_t M, int64_t K, int64_t N);
 size_t ws_w8a8_quant_linear(int64_t M, int64_t K, int64_t N);
 size_t ws_fp8_group_einsum(int64_t T, int64_t D, int64_t N, int64_t G);
 size_t ws_w8a8_grouped_linear(int64_t R, int64_t K, int64_t N, int64_t E);
+// Per-token INT8 quant; trigger: let the next kernel launch before this one
+// finishes (only where the output is activations).
+fq_status quant_int8_launch(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx, fq_stream_t stream,
+                            bool trigger);
 size_t ws_mxfp8_linear(int64_t M, int64_t K, int64_t N);
 constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 }  // namespace fq

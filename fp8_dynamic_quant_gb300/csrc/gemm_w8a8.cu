@@ -1738,7 +1738,8 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
     const bool pdl = pdl_enabled();
     return cuda_status(launch_gemm<8, 14, false, true>(&tw_map, &tw_map, p, int(tiles), s, pdl));
   }
-  if ((st = dynamic_quant_int8(x, M, K, xq, sx, stream)) != FQ_OK) return st;
+  // the quant's output is this call's activations: the GEMM may launch early
+  if ((st = quant_int8_launch(x, M, K, xq, sx, stream, true)) != FQ_OK) return st;
   if (N == 0) return FQ_OK;
   if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(M) * size_t(N) * 2, s));
   return run_w8a8_dense(xq, sx, M, K, w_nk, sw, N, y, reinterpret_cast<uint32_t*>(w8),

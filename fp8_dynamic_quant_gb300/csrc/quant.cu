@@ -39,13 +39,18 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 // One CTA per row (grid-stride over rows).  Each thread keeps up to VPT
 // 16-byte vectors (8 bf16) of the row in registers between the absmax pass
 // and the quant pass; longer rows re-read the remainder (L2-resident).
+// trigger: let the next kernel launch early.  Only for outputs that are
+// activations: a dependent may read its weight operand before its own wait,
+// so a call whose output could be that weight (the public entry point: a
+// per-row quant of W is the per-channel weight quant) lets the next kernel
+// start only once it has finished.
 template <int VPT>
 __global__ void __launch_bounds__(256) dynamic_quant_int8_kernel(const uint4* __restrict__ x, int64_t M,
                                                                   int64_t K8, uint2* __restrict__ q,
-                                                                  float* __restrict__ s) {
+                                                                  float* __restrict__ s, int trigger) {
   __shared__ float red[32];
   pdl_wait();
-  pdl_launch_dependents();
+  if (trigger) pdl_launch_dependents();
   const int tid = threadIdx.x, nt = blockDim.x;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x) {
     const uint4* xr = x + row * K8;
@@ -472,8 +477,10 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const uint4* __restr
 // (r % 32) * 16 + ((r % 128) / 32) * 4 + b % 4.
 __global__ void __launch_bounds__(256) quant_mxfp8_kernel(const uint4* __restrict__ x, int64_t R, int64_t K8,
                                                           uint2* __restrict__ q, uint8_t* __restrict__ sf) {
+  // no early trigger: the output is the weight operand of a linear as often
+  // as its activations, and a dependent may read its weights before its own
+  // wait
   pdl_wait();
-  pdl_launch_dependents();
   const int64_t total = R * K8, KB = K8 / 16;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t span = (total + 31) / 32 * 32;  // whole warps stay in the loop together
@@ -588,8 +595,8 @@ using namespace fq;
 
 // ================================================================ entry points
 
-extern "C" __attribute__((visibility("default"))) fq_status dynamic_quant_int8(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx,
-                                        fq_stream_t stream) {
+fq_status fq::quant_int8_launch(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx, fq_stream_t stream,
+                            bool trigger) {
   if (M < 0 || K < 0 || K % 16 || K > (int64_t(1) << 30) || M > (int64_t(1) << 40)) return FQ_ERR_SHAPE;
   if (M == 0) return FQ_OK;
   if (!x || !xq || !sx) return FQ_ERR_NULL;
@@ -606,15 +613,21 @@ extern "C" __attribute__((visibility("default"))) fq_status dynamic_quant_int8(c
   cudaError_t e;
   auto xp = reinterpret_cast<const uint4*>(x);
   auto qp = reinterpret_cast<uint2*>(xq);
+  const int tr = trigger ? 1 : 0;
   if (vpt <= 1)
-    e = launch(dynamic_quant_int8_kernel<1>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+    e = launch(dynamic_quant_int8_kernel<1>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
   else if (vpt <= 2)
-    e = launch(dynamic_quant_int8_kernel<2>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+    e = launch(dynamic_quant_int8_kernel<2>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
   else if (vpt <= 4)
-    e = launch(dynamic_quant_int8_kernel<4>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+    e = launch(dynamic_quant_int8_kernel<4>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
   else
-    e = launch(dynamic_quant_int8_kernel<8>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx);
+    e = launch(dynamic_quant_int8_kernel<8>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
   return cuda_status(e);
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status dynamic_quant_int8(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx,
+                                        fq_stream_t stream) {
+  return quant_int8_launch(x, M, K, xq, sx, stream, false);
 }
 
 extern "C" __attribute__((visibility("default"))) fq_status swiglu_quant_int8(const uint16_t* gu, int64_t rows, int64_t I, int8_t* hq, float* sh,

@@ -45,6 +45,16 @@
  *     recorded in a device error word and read with fq_device_error().
  *   - The library needs an sm_103 device; anything else returns
  *     FQ_ERR_UNSUPPORTED_DEVICE.
+ *   - Kernels are launched with programmatic dependent launch (unless the
+ *     environment sets FQ_PDL=0): a linear may start while the previous
+ *     kernel on the stream is still running and stream its WEIGHTS (and
+ *     weight scales) before it waits for that kernel; everything else it
+ *     reads after the wait.  The calls whose output can be a weight operand
+ *     (dynamic_quant_int8, quant_mxfp8, fq_quantize_weight_fp8_block) let
+ *     the next kernel start only once they have finished, so weights they
+ *     write are complete.  Weights written by other code that also launches
+ *     its kernels early must be separated from the linear by an ordinary
+ *     stream operation.
  */
 #ifndef FQ_H_
 #define FQ_H_

@@ -192,6 +192,31 @@ def test_fused_one_launch_forced_small_n_and_ties(monkeypatch, capfd):
     assert np.array_equal(y, want) and np.array_equal(y_plain, want)
 
 
+@pytest.mark.parametrize("K,N", [(1024, 8192), (1024, 32768), (4096, 1024)])
+def test_linear_right_after_weight_quant(K, N):
+    """Per-channel weight quant (dynamic_quant_int8 on W's rows) launched right before the linear with
+    nothing else on the stream in between: the linear streams its weights before it waits on the
+    previous kernel, so the weight quant must let it start only once it has finished."""
+    dev = torch.device("cuda")
+    M = 4
+    x = synth.activations(M, K, 91)
+    q, s = oi8.dynamic_quant_int8(x)
+    qd, sd = np_to_dev(q), np_to_dev(s)
+    wq = torch.empty(N, K, dtype=torch.int8, device=dev)
+    swq = torch.empty(N, dtype=torch.float32, device=dev)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    ws = fq.new_workspace(fq.workspace_bytes(fq.OP_W8A8_LINEAR, M, K, N), dev)
+    for i in range(3):
+        wf = synth.activations(N, K, 900 + i + N)
+        wd = bf16_to_dev(wf)
+        torch.cuda.synchronize()
+        fq.dynamic_quant_int8(wd, wq, swq)
+        fq.w8a8_linear(qd, sd, wq, swq, y=y, ws=ws)
+        torch.cuda.synchronize()
+        oq, os_ = oi8.dynamic_quant_int8(wf)
+        assert np.array_equal(bf16_to_np(y), oi8.w8a8_linear(q, s, oq, os_))
+
+
 def test_workspace_counters_return_to_zero():
     c = synth.int8_linear_case(9, 4096, 1024, 11)
     q, s = oi8.dynamic_quant_int8(c["x"])

@@ -96,3 +96,26 @@ def test_many_iterations_per_cta_no_drain_stall():
     oqw, osw = mx.quant_mxfp8(w[cols])
     want = mx.mxfp8_linear(oqx, osx, oqw, osw)
     assert within_tol(bf16_to_np(y)[:, cols], want)
+
+
+def test_linear_right_after_weight_quant():
+    """quant_mxfp8 of the weights launched right before mxfp8_linear with nothing else on the stream in
+    between: the linear streams its weights and their scales before it waits on the previous kernel."""
+    dev = torch.device("cuda")
+    M, K, N = 4, 4096, 1024
+    x = synth.activations(M, K, 95)
+    qx, sx = fq.quant_mxfp8(bf16_to_dev(x))
+    oqx, osx = mx.quant_mxfp8(x)
+    qw = torch.empty(N, K, dtype=torch.float8_e4m3fn, device=dev)
+    wsf = torch.empty((N // 128, K // 128, 512), dtype=torch.uint8, device=dev)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    ws = fq.new_workspace(fq.workspace_bytes(fq.OP_MXFP8_LINEAR, M, K, N), dev)
+    for i in range(3):
+        w, (oqw, osw) = weights(N, K, 700 + i)
+        wd = bf16_to_dev(w)
+        torch.cuda.synchronize()
+        fq.quant_mxfp8(wd, qw, wsf)
+        fq.mxfp8_linear(qx, sx, qw, wsf, y=y, ws=ws)
+        torch.cuda.synchronize()
+        assert within_tol(bf16_to_np(y), mx.mxfp8_linear(oqx, osx, oqw, osw))
+    assert fq.device_error() == (0, 0)
