@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
           do_epi = s_flag != 0;
           if (do_epi) {
             // add the other contributors' partials; U slots in flight at once
-            constexpr int U = NT <= 2 ? 8 : (NT <= 4 ? 4 : 1);
+            constexpr int U = NT <= 2 ? 8 : (NT <= 4 && CW <= 8 ? 4 : 1);
             const int c0 = cta_of(rb, G, tile * KB), c1 = cta_of(rb, G, tile * KB + KB - 1);
             for (int cb = c0; cb <= c1; cb += U) {
               int32_t v[U][NT][4];
@@ -1550,16 +1550,16 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   // Schedule.  When tiles of 224 weight rows (14 consumer warps) give between
   // 3/4 of and one tile per SM, every CTA streams one whole tile: no split-K,
   // no partial sums.  Otherwise 128-row tiles are split stream-K over one CTA
-  // per SM.  (224-row tiles need MT <= 16 to fit the register file.)
+  // per SM.  (224-row tiles need MT <= 32 to fit the register file.)
   const int64_t tiles224 = ((N + 223) / 224) * m_tiles;
-  bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
+  bool data_parallel = mt <= 32 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
   // Few tiles (small N): 32-row tiles, each split over K by a cluster of 4 CTAs
   // with a distributed-shared-memory reduction, when that fills >= 1/2 the GPU
   // (every token tile: with its k-split warps it beats the tcgen05 kernel at 64).
   const int64_t ctas_cl = ((N + 31) / 32) * m_tiles * 4;
   bool cluster = !data_parallel && ctas_cl <= d.sm_count && ctas_cl * 2 >= d.sm_count && KB >= 4;
   const int force = forced_schedule();
-  if (force == SCHED_DP && mt <= 16 && tiles224 <= kMaxGrid) {
+  if (force == SCHED_DP && mt <= 32 && tiles224 <= kMaxGrid) {
     data_parallel = true;
     cluster = false;
   } else if (force == SCHED_CLUSTER && KB >= 4 && ctas_cl <= (int64_t(1) << 30)) {
@@ -1648,7 +1648,9 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     e = mt_run == 32 ? launch_umma_gemm<32, false>(tw, tx, &tx16, &tx32, p, grid, s, pdl)
                      : launch_umma_gemm<64, false>(tw, tx, &tx16, &tx32, p, grid, s, pdl);
   } else if (data_parallel) {
-    e = mt == 8 ? launch_gemm<8, 14, false>(tw, tx, p, grid, s, pdl) : launch_gemm<16, 14, false>(tw, tx, p, grid, s, pdl);
+    e = mt == 8    ? launch_gemm<8, 14, false>(tw, tx, p, grid, s, pdl)
+        : mt == 16 ? launch_gemm<16, 14, false>(tw, tx, p, grid, s, pdl)
+                   : launch_gemm<32, 14, false>(tw, tx, p, grid, s, pdl);
   } else {
     switch (mt) {
       case 8: e = launch_gemm<8, 8, false>(tw, tx, p, grid, s, pdl); break;
