@@ -31,3 +31,9 @@ def within_tol(got_bits, want_bits, rtol=1e-2, atol=1e-3):
     err = np.abs(g - w) - (atol + rtol * np.abs(w))
     i = int(np.argmax(err)) if err.size else 0
     return bool(err.size == 0 or err.max() <= 0), (i, g.ravel()[i] if err.size else None, w.ravel()[i] if err.size else None)
+
+
+def assert_within_tol(got_bits, want_bits, rtol=1e-2, atol=1e-3):
+    """Assert within_tol, reporting the worst element (index, got, want) on failure."""
+    ok, info = within_tol(got_bits, want_bits, rtol, atol)
+    assert ok, info

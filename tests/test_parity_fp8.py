@@ -12,7 +12,7 @@ import torch
 from oracle import codecs, fp8 as of8
 from fp8_dynamic_quant_gb300 import synth
 import fp8_dynamic_quant_gb300 as fq
-from _util import bf16_to_dev, bf16_to_np, e4m3_to_np, e4m3_to_dev, np_to_dev, within_tol
+from _util import assert_within_tol, bf16_to_dev, bf16_to_np, e4m3_to_np, e4m3_to_dev, np_to_dev, within_tol
 
 pytestmark = pytest.mark.gpu
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
@@ -238,4 +238,4 @@ def test_tiny_group_scale_byte_zero():
     yf = fq.fp8_group_einsum(xq, s32, fq.SCALE_FP32, wq, sw)
     assert torch.equal(yp.view(torch.int16), yf.view(torch.int16))
     want = of8.fp8_group_einsum(oxq, of8.unpack_scales(ost, T, D // 128), owq, osw)
-    assert within_tol(bf16_to_np(yp), want)
+    assert_within_tol(bf16_to_np(yp), want)

@@ -12,7 +12,7 @@ import torch
 from oracle import codecs, mx
 from fp8_dynamic_quant_gb300 import synth
 import fp8_dynamic_quant_gb300 as fq
-from _util import bf16_to_dev, bf16_to_np, e4m3_to_np, within_tol
+from _util import assert_within_tol, bf16_to_dev, bf16_to_np, e4m3_to_np, within_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,7 @@ def test_linear_within_tolerance(M, K, N):
     y = fq.mxfp8_linear(qx, sx, qw, wsf)
     oqx, osx = mx.quant_mxfp8(x)
     want = mx.mxfp8_linear(oqx, osx, oqw, osw)
-    assert within_tol(bf16_to_np(y), want)
+    assert_within_tol(bf16_to_np(y), want)
     assert fq.device_error() == (0, 0)
 
 
@@ -95,7 +95,7 @@ def test_many_iterations_per_cta_no_drain_stall():
     oqx, osx = mx.quant_mxfp8(x)
     oqw, osw = mx.quant_mxfp8(w[cols])
     want = mx.mxfp8_linear(oqx, osx, oqw, osw)
-    assert within_tol(bf16_to_np(y)[:, cols], want)
+    assert_within_tol(bf16_to_np(y)[:, cols], want)
 
 
 def test_linear_right_after_weight_quant():
@@ -117,5 +117,5 @@ def test_linear_right_after_weight_quant():
         fq.quant_mxfp8(wd, qw, wsf)
         fq.mxfp8_linear(qx, sx, qw, wsf, y=y, ws=ws)
         torch.cuda.synchronize()
-        assert within_tol(bf16_to_np(y), mx.mxfp8_linear(oqx, osx, oqw, osw))
+        assert_within_tol(bf16_to_np(y), mx.mxfp8_linear(oqx, osx, oqw, osw))
     assert fq.device_error() == (0, 0)
