@@ -17,12 +17,17 @@
 //    |partial| <= 1024*127*127 < 2^24) the fp32 accumulator is folded into an
 //    int32 one: the GEMM stays exact.  int8 -> f16 is a byte permute onto the
 //    f16 pattern of 1024 + (q + 128) followed by one f16x2 subtract.
-//  * Operand staging: a producer warp streams 128x128-byte weight boxes and
-//    MTx128-byte activation boxes with TMA (cp.async.bulk.tensor, 128-byte
-//    swizzle) into a multi-stage mbarrier ring; eight consumer warps each own
-//    16 channels.  Because the K order inside a sum is free, each lane reads
-//    one contiguous 16-byte chunk per row and the same physical-to-logical K
+//  * Operand staging: a producer warp streams (16*CW)x128-byte weight boxes
+//    and MTx128-byte activation boxes with TMA (cp.async.bulk.tensor,
+//    128-byte swizzle) into a multi-stage mbarrier ring; CW consumer warps
+//    (8, or 14 for 224-row tiles) each own 16 channels, and one converter
+//    warp turns each stage's activations into f16 B fragments once for all
+//    of them.  Because the K order inside a sum is free, each lane reads one
+//    contiguous 16-byte chunk per row and the same physical-to-logical K
 //    permutation is applied to both operands, so no shuffles are needed.
+//  * Small N (K=4096, N=1024): 4-CTA clusters split K and reduce through
+//    distributed shared memory; 64-token tiles on wide N and the MoE: the
+//    tcgen05 kernel below.
 //  * Scheduling: stream-K.  The (tile, k-block) iteration space is cut into
 //    equal contiguous ranges, one per CTA (one CTA per SM), which balances
 //    any (M, N, K) across all 152 SMs - the role the pages give to baseM /
@@ -30,10 +35,15 @@
 //    A CTA's first and last tiles may be partial: their int32 partials go to
 //    per-CTA workspace slots, and the last CTA to finish a tile (counted with
 //    an atomic per tile) adds them up and runs the dequant epilogue.  Integer
-//    sums make the result independent of that order.
+//    sums make the result independent of that order.  When 224-row tiles
+//    give 3/4 to 1 tile per SM (up to 32 tokens), each CTA streams one whole
+//    tile instead, and the fused op with up to 8 tokens is one launch whose
+//    CTAs quantize the activations themselves.
 //  * Weights are read with an L2 evict-first hint; activations evict-last.
 //  * Programmatic dependent launch: weight loads for the first stages are
-//    issued before griddepcontrol.wait, overlapping the previous kernel.
+//    issued at kernel entry, before griddepcontrol.wait, overlapping the
+//    previous kernel.  (Library calls that can write a weight operand let
+//    the next kernel start only once they have finished.)
 #include <cuda_fp16.h>
 
 #include <cstdio>
