@@ -162,6 +162,29 @@ def test_einsum_within_tolerance_and_scale_formats_identical(T, G, D, N):
     assert ok, info
 
 
+@pytest.mark.parametrize("sched", ["dp", "streamk"])
+@pytest.mark.parametrize("T,G,D,N", [(1, 8, 4096, 1024), (5, 8, 4096, 1024), (16, 8, 4096, 1024),
+                                     (40, 8, 4096, 1024), (3, 3, 640, 384), (9, 2, 384, 256)])
+def test_einsum_both_schedules(sched, T, G, D, N, monkeypatch):
+    """Whole 64-row tiles, one per CTA (dp, taken only when forced), and 128-row tiles split stream-K:
+    each within tolerance, packed and fp32 scales identical, repeat calls identical."""
+    monkeypatch.setenv("FQ_FORCE_SCHEDULE", sched)
+    x = synth.group_activations(T, G, D, 7300 + T + G)
+    owq, osw, wq, sw = einsum_weights(G, N, D, 9)
+    xg = bf16_to_dev(x)
+    xq, st = fq.quant_fp8_group_ue8m0_packed(xg)
+    _, s32 = fq.quant_fp8_group_fp32(xg)
+    y1 = fq.fp8_group_einsum(xq, st, fq.SCALE_UE8M0_PACKED, wq, sw)
+    y2 = fq.fp8_group_einsum(xq, st, fq.SCALE_UE8M0_PACKED, wq, sw)
+    yf = fq.fp8_group_einsum(xq, s32, fq.SCALE_FP32, wq, sw)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), yf.view(torch.int16))
+    oxq, ost = of8.quant_fp8_group_ue8m0_packed(x)
+    assert_within_tol(bf16_to_np(y1), of8.fp8_group_einsum(oxq, of8.unpack_scales(ost, T, D // 128), owq, osw))
+    assert fq.device_error() == (0, 0)
+
+
 def test_einsum_integer_case_exact():
     """Unit scales and small-integer E4M3 operands: every sum is an exact integer."""
     T, G, D, N = 5, 2, 256, 128
