@@ -75,6 +75,20 @@ def bytes_einsum(T, G, D, N):
 
 
 # ---------------------------------------------------------------- peaks
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x: the job takes as long as its slowest rank."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(bytes_per_step_per_rank, ms_per_step, world):
+    """GB/s of the whole job: every rank (an independent replica) moves its own step's bytes in the
+    slowest rank's step time."""
+    return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -277,13 +291,11 @@ def run_fq(args, rank, world, local_rank):
     clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, dist, dev)
     group_ms = [sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K_steps)) / K_steps for i in range(len(graphs))]
     ms_per_step = total_ms / K_steps
     sb = step_bytes()
-    value = world * sb / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_value(sb, ms_per_step, world)
 
     group_report = {}
     for (name, _, nbytes, nl), ms in zip(graphs, group_ms):
