@@ -692,7 +692,8 @@ def run_profile_case(name):
     """Run one op of the workload a few times, untimed, as a target for a profiler.
 
     gemm_K1024_N32768 / gemm_K4096_N1024: the W8A8 GEMM once per M of the sweep,
-    each call on its own weight copy; einsum_T<T>: the block-scaled FP8 einsum
+    each call on its own weight copy; fused_K1024_N32768: the fused quant + GEMM
+    the same way; einsum_T<T>: the block-scaled FP8 einsum
     (G=8, D=4096, N=1024) three times; int8_quant_M16384: the per-token quant
     at M=16384, K=4096 twice; fp8_group_quant_T4096: the group quant with packed
     UE8M0 scales at T=4096, G=8, D=4096 twice.  Prints one status line."""
@@ -716,6 +717,14 @@ def run_profile_case(name):
             sw = synth.uniform_f32_device((N,), 1e-3, 1e-2, SEED + 7 + 100 * i + N, dev)
             xq, sx = fq.dynamic_quant_int8(bf(synth.activations(M, K, SEED + 1000 + M + K)))
             fq.w8a8_linear(xq, sx, w, sw, ws=ws)
+            launches += 1
+    elif name == "fused_K1024_N32768":
+        K, N = 1024, 32768
+        ws = fq.new_workspace(fq.workspace_bytes(fq.OP_W8A8_QUANT_LINEAR, 64, K, N), dev)
+        for i, M in enumerate(MS):
+            w = synth.uniform_int8_device((N, K), SEED + 100 * i + K + N, dev)
+            sw = synth.uniform_f32_device((N,), 1e-3, 1e-2, SEED + 7 + 100 * i + N, dev)
+            fq.w8a8_quant_linear(bf(synth.activations(M, K, SEED + 1000 + M + K)), w, sw, ws=ws)
             launches += 1
     elif name.startswith("einsum_T"):
         T, G, D, N = int(name[len("einsum_T"):]), 8, 4096, 1024
