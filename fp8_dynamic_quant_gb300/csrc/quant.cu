@@ -95,8 +95,49 @@ __global__ void __launch_bounds__(256) dynamic_quant_int8_kernel(const uint4* __
 
 // ---------------------------------------------------------------- a7: SwiGLU + INT8
 
-// h = bf16_RN(fp32(silu(g)) * u), silu(g) = g / (1 + exp(-g)); then the
-// per-token quant of h.  One CTA per row; VPT vectors of 8 outputs cached.
+// h = bf16_RN(fp32(s * u)) with s = fp32_RN(silu(g)), silu(g) = g / (1 + exp(-g))
+// rounded once to fp32 (the exact value's rounding); then the per-token
+// quant of h.  One CTA per row; VPT vectors of 8 outputs cached.
+//
+// Fast path: s is estimated in fp32 with expf.  For |g| <= 64 that estimate
+// is within 5 units in the last place of the correctly rounded s (expf's
+// documented 2-ulp bound plus at most three fp32 roundings, all on normal
+// numbers), so the correctly rounded s lies in the bracket of +-16 ulp steps
+// around it (twice the bound, for a bracket that crosses a power of two).
+// h is a monotone function of s for a fixed u (two monotone roundings of a
+// product), so when both ends of the bracket give the same h, that h is
+// exact.  Otherwise (h within a few fp32 ulps of a bf16 rounding boundary,
+// about 5e-4 of elements, or |g| > 64) s is recomputed as the fp64 quotient
+// g / (1 + exp(-g)) rounded once to fp32.  For all but 32 bf16 values of g
+// (all with |g| < 6e-5) silu(g) lies more than 2^-45 (relative) from every
+// fp32 rounding midpoint, far beyond the fp64 quotient's error, so this is
+// the correctly rounded s; for those 32 the fp64 steps are the same IEEE
+// operations on an argument whose exp any fp64 library rounds correctly.
+// Tests check every bf16 g.
+__device__ __forceinline__ uint16_t swiglu_h_bits(float g, float u) {
+  // silu(g) = g / (1 + e^-g); for g < 0 the same value as g e^g / (1 + e^g),
+  // which does not overflow for large |g|
+  float sg;
+  if (g >= 0.0f) {
+    sg = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  } else {
+    const float e = expf(g);
+    sg = __fdiv_rn(__fmul_rn(g, e), __fadd_rn(1.0f, e));
+  }
+  if (fabsf(g) <= 64.0f) {
+    const uint32_t b = __float_as_uint(sg);
+    const uint32_t sign = b & 0x80000000u, mag = b & 0x7FFFFFFFu;
+    const float s_lo = __uint_as_float(sign | (mag > 16u ? mag - 16u : 0u));
+    const float s_hi = __uint_as_float(sign | (mag + 16u));
+    const uint16_t h_lo = f32_to_bf16_bits(__fmul_rn(s_lo, u));
+    const uint16_t h_hi = f32_to_bf16_bits(__fmul_rn(s_hi, u));
+    if (h_lo == h_hi) return h_lo;
+  }
+  const double gd = double(g);
+  const float s = __double2float_rn(__ddiv_rn(gd, __dadd_rn(1.0, exp(-gd))));
+  return f32_to_bf16_bits(__fmul_rn(s, u));
+}
+
 __device__ __forceinline__ void swiglu8(const uint4& gv, const uint4& uv, float h[8], uint4* hbits) {
   float g[8], u[8];
   unpack8(gv, g);
@@ -104,16 +145,7 @@ __device__ __forceinline__ void swiglu8(const uint4& gv, const uint4& uv, float 
   uint32_t hb[4];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    // silu(g) = g / (1 + e^-g); for g < 0 the same value as g e^g / (1 + e^g),
-    // which does not overflow for large |g|
-    float sg;
-    if (g[i] >= 0.0f) {
-      sg = __fdiv_rn(g[i], __fadd_rn(1.0f, expf(-g[i])));
-    } else {
-      const float e = expf(g[i]);
-      sg = __fdiv_rn(__fmul_rn(g[i], e), __fadd_rn(1.0f, e));
-    }
-    const uint16_t b = f32_to_bf16_bits(__fmul_rn(sg, u[i]));
+    const uint16_t b = swiglu_h_bits(g[i], u[i]);
     h[i] = __uint_as_float(uint32_t(b) << 16);
     if (i & 1)
       hb[i >> 1] |= uint32_t(b) << 16;

@@ -15,8 +15,11 @@ Readings for silent points:
     this identical to quantizing the gathered copies);
   * gate/up layout: the first I columns of the W13 output are the gate g,
     the last I the up projection u;
-  * h = bf16_RN(fp32(silu(g)) * u) with silu(g) = g / (1 + exp(-g)) taken in
-    float64 and rounded once to fp32; then the INT8 per-token quant of h;
+  * h = bf16_RN(fp32(s * u)) with s = fp32_RN(silu(g)), silu(g) =
+    g / (1 + exp(-g)): the exact value rounded once to fp32, evaluated as the
+    float64 quotient rounded once to fp32 (for every bf16 g the two agree; a
+    test checks all 65536 values against a 200-bit evaluation); then the INT8
+    per-token quant of h;
   * combine: out[t] = bf16_RN(sum over slots j = 0..topk-1, in slot order,
     of fp32(w[t, j] * y[row(t, j)])), an fp32 running sum.
 """
@@ -62,14 +65,19 @@ def w8a8_grouped_linear(q, s, offsets, w_enk, sw_en):
     return y
 
 
+def silu_f32(g):
+    """s = fp32_RN(g / (1 + exp(-g))) for fp32 (bf16-valued) g, via the float64 quotient."""
+    g = np.asarray(g, np.float32).astype(np.float64)
+    with np.errstate(over="ignore"):                    # exp(-g) = inf for g < -709: silu -> -0
+        return (g / (1.0 + np.exp(-g))).astype(np.float32)
+
+
 def swiglu_bf16(gu_bf16):
     """h = bf16_RN(fp32(silu(g)) * u), g = first half of the columns, u = second."""
     gu = bf16_to_f32(np.asarray(gu_bf16, np.uint16))
     I = gu.shape[1] // 2
-    g = gu[:, :I].astype(np.float64)
+    silu = silu_f32(gu[:, :I])
     u = gu[:, I:]
-    with np.errstate(over="ignore"):                    # exp(-g) = inf for g < -709: silu -> -0
-        silu = (g / (1.0 + np.exp(-g))).astype(np.float32)
     return f32_to_bf16((silu * u).astype(np.float32))
 
 

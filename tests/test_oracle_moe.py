@@ -70,3 +70,50 @@ def test_combine_closed_form():
     # pair 0 -> row 1, pair 1 -> row 3, pair 2 -> row 2, pair 3 -> row 0
     assert out.tolist() == [[0.5 * 10 + 0.25 * 0.5] * 0 + [5.125, 10.125, 15.125, 20.125],
                             [-2 + 1, -2 + 2, -2 + 3, -2 + 4]]
+
+
+def _correctly_rounded_silu_f32(g_values):
+    """fp32 bit patterns of silu(g) = g / (1 + exp(-g)) evaluated with 200-bit
+    arithmetic and rounded once to fp32 (subnormals included, ties to even)."""
+    mpmath = __import__("pytest").importorskip("mpmath")
+    out = np.empty(len(g_values), np.uint32)
+    with mpmath.workprec(200):
+        for i, g in enumerate(g_values):
+            g = float(g)
+            sign = 0x80000000 if np.signbit(np.float32(g)) else 0
+            if g == 0.0:
+                out[i] = sign
+                continue
+            gm = mpmath.mpf(g)
+            s = abs(gm / (1 + mpmath.exp(-gm)))
+            e = int(mpmath.floor(mpmath.log(s, 2))) if s > 0 else -200
+            ulp = mpmath.mpf(2) ** max(e - 23, -149)
+            q = s / ulp
+            n = int(mpmath.floor(q))
+            frac = q - n
+            if frac > 0.5 or (frac == 0.5 and n % 2 == 1):
+                n += 1
+            mag = np.float32(float(n * ulp))       # n * ulp has <= 25 significant bits: exact
+            out[i] = np.uint32(mag.view(np.uint32)) | sign
+    return out
+
+
+def test_silu_f32_is_the_correctly_rounded_silu_for_every_bf16():
+    """The oracle's float64 quotient rounded to fp32 equals the exact silu
+    rounded once to fp32 for every finite bf16 input (infinities and NaN are
+    outside the contract: the gate is a finite GEMM output)."""
+    bits = np.arange(65536, dtype=np.uint32) << 16
+    g = bits.view(np.float32)
+    fin = np.isfinite(g)
+    got = moe.silu_f32(g[fin]).view(np.uint32)
+    want = _correctly_rounded_silu_f32(g[fin])
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(g[fin][i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def test_silu_near_midpoint_cases_hand_derived():
+    """g = -2^-24: silu(g) = -2^-25 (1 - 2^-25 + 2^-72/48 + ...) sits 2^-76.6 above the
+    magnitude midpoint 2^-25 - 2^-50, so it rounds to -2^-25; g = 2^-23:
+    silu(g) = 2^-24 (1 + 2^-24 - ...) rounds to 2^-24 (the midpoint is 2^-24 (1 + 2^-24))."""
+    assert moe.silu_f32(np.float32(-2.0 ** -24)).view(np.uint32) == np.float32(-2.0 ** -25).view(np.uint32)
+    assert moe.silu_f32(np.float32(2.0 ** -23)) == np.float32(2.0 ** -24)
