@@ -15,7 +15,8 @@ __all__ = [
     "quant_fp8_group_ue8m0_packed", "quant_fp8_group_fp32", "pack_scales_ue8m0", "quantize_weight_fp8_block",
     "fp8_group_einsum", "scale_view", "moe_sort", "moe_gather_rows_i8", "w8a8_grouped_linear",
     "swiglu_quant_int8", "moe_combine", "device_error", "selftest_wait_timeout", "rmsnorm_quant_int8",
-    "rmsnorm_quant_fp8_ue8m0_packed", "quant_mxfp8", "mxfp8_linear", "OP_MXFP8_LINEAR", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
+    "rmsnorm_quant_fp8_ue8m0_packed", "check_device_error", "repack_weight_kmajor_i8",
+    "repack_weight_kmajor_fp8", "quant_mxfp8", "mxfp8_linear", "OP_MXFP8_LINEAR", "workspace_bytes", "SCALE_UE8M0_PACKED", "SCALE_FP32",
     "OP_W8A8_LINEAR", "OP_W8A8_QUANT_LINEAR", "OP_FP8_GROUP_EINSUM", "OP_MOE_SORT", "OP_W8A8_GROUPED_LINEAR",
 ]
 
@@ -33,6 +34,9 @@ _SIGS = {
     "fq_status_string": ([_I32], ctypes.c_char_p),
     "fq_last_cuda_error": ([], _I32),
     "fq_device_error": ([_P, _U32P], _I32),
+    "fq_check_device_error": ([_P], _I32),
+    "fq_repack_weight_kmajor_i8": ([_P, _I64, _I64, _I64, _P, _P], _I32),
+    "fq_repack_weight_kmajor_fp8": ([_P, _I64, _I64, _I64, _P, _P], _I32),
     "fq_selftest_wait_timeout": ([ctypes.c_uint64, _I32, _P], _I32),
     "rmsnorm_quant_int8": ([_P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P], _I32),
     "rmsnorm_quant_fp8_ue8m0_packed": ([_P, _P, ctypes.c_float, _I64, _I64, _P, _P, _P], _I32),
@@ -136,6 +140,32 @@ def device_error():
     w = ctypes.c_uint32(0)
     st = lib().fq_device_error(_stream(), ctypes.byref(w))
     return st, w.value
+
+
+def check_device_error():
+    """Synchronises the current stream; returns the status of the device error word (and clears it)."""
+    return int(lib().fq_check_device_error(_stream()))
+
+
+def repack_weight_kmajor_i8(w_kn, out=None):
+    """Logical int8 weights [K, N] or [B, K, N] -> K-major storage [N, K] / [B, N, K] (load time)."""
+    _cuda(w_kn, torch.int8, "w_kn")
+    squeeze = w_kn.dim() == 2
+    w3 = w_kn.unsqueeze(0) if squeeze else w_kn
+    B, K, N = w3.shape
+    out = torch.empty((B, N, K), dtype=torch.int8, device=w_kn.device) if out is None else out.view(B, N, K)
+    _check("fq_repack_weight_kmajor_i8", lib().fq_repack_weight_kmajor_i8(_ptr(w3), B, K, N, _ptr(out), _stream()))
+    return out[0] if squeeze else out
+
+
+def repack_weight_kmajor_fp8(w_gdn, out=None):
+    """Logical E4M3 einsum weights [G, D, N] -> K-major storage [G, N, D] (load time)."""
+    _cuda(w_gdn, torch.float8_e4m3fn, "w_gdn")
+    G, D, N = w_gdn.shape
+    out = torch.empty((G, N, D), dtype=torch.float8_e4m3fn, device=w_gdn.device) if out is None else out
+    _check("fq_repack_weight_kmajor_fp8",
+           lib().fq_repack_weight_kmajor_fp8(_ptr(w_gdn), G, D, N, _ptr(out), _stream()))
+    return out
 
 
 def selftest_wait_timeout(budget_ns=1_000_000, arrive=False):

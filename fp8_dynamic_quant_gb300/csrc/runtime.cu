@@ -187,7 +187,7 @@ extern "C" __attribute__((visibility("default"))) const char* fq_status_string(i
     case FQ_ERR_CUDA: return "CUDA call failed (see fq_last_cuda_error)";
     case FQ_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
     case FQ_ERR_DEVICE_INPUT: return "device input broke the contract (e.g. expert id out of range)";
-    case FQ_ERR_ARG: return "unknown enum argument";
+    case FQ_ERR_ARG: return "invalid argument value (unknown enum, bad eps, overlapping buffers)";
     default: return "unknown status";
   }
 }
@@ -207,6 +207,10 @@ extern "C" __attribute__((visibility("default"))) fq_status fq_device_error(fq_s
   if (w & DEVERR_TIMEOUT) return FQ_ERR_DEVICE_TIMEOUT;
   if (w) return FQ_ERR_DEVICE_INPUT;
   return FQ_OK;
+}
+
+extern "C" __attribute__((visibility("default"))) fq_status fq_check_device_error(fq_stream_t stream) {
+  return fq_device_error(stream, nullptr);
 }
 
 extern "C" __attribute__((visibility("default"))) size_t fq_workspace_bytes(int op, int64_t a, int64_t b, int64_t c, int64_t d) {

@@ -79,7 +79,7 @@ typedef enum fq_status {
   FQ_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed; see fq_last_cuda_error() */
   FQ_ERR_DEVICE_TIMEOUT = 7,     /* a bounded device wait gave up (reported by fq_device_error) */
   FQ_ERR_DEVICE_INPUT = 8,       /* device data broke the contract, e.g. expert id out of range */
-  FQ_ERR_ARG = 9                 /* an enum argument has an unknown value */
+  FQ_ERR_ARG = 9                 /* an argument value is invalid: unknown enum, non-finite eps, overlapping buffers */
 } fq_status;
 
 /* Text for a status code; never NULL. */
@@ -92,6 +92,11 @@ int fq_last_cuda_error(void);
  * current device.  Returns FQ_OK, FQ_ERR_DEVICE_TIMEOUT or
  * FQ_ERR_DEVICE_INPUT; *detail (nullable) receives the raw word. */
 fq_status fq_device_error(fq_stream_t stream, uint32_t* detail);
+
+/* The same check without the raw word: synchronises `stream`, reads and
+ * clears the device error word, and returns FQ_OK, FQ_ERR_DEVICE_TIMEOUT or
+ * FQ_ERR_DEVICE_INPUT (or FQ_ERR_CUDA if the synchronisation failed). */
+fq_status fq_check_device_error(fq_stream_t stream);
 
 /* Failure-detection self-test of the bounded device waits (no counterpart
  * in the pages; it exercises the same wait loop every pipelined kernel uses).
@@ -121,6 +126,30 @@ typedef enum fq_op {
   FQ_OP_MXFP8_LINEAR = 6
 } fq_op;
 size_t fq_workspace_bytes(int op, int64_t a, int64_t b, int64_t c, int64_t d);
+
+/* --------------------------------------------------- load-time weight layout */
+
+/* One-time repack of weights to the K-major layout every linear here reads.
+ * [W8A8] section 4: weights are cast once at load time to the layout the
+ * matmul streams best (npu_format_cast to FRACTAL_NZ there); here a logical
+ * W[k, n] is stored as w_nk[n * K + k], so each TMA box is a run of output
+ * channels with contiguous K bytes.  Untimed, off the decode path.
+ *   w_kn : int8 [B, K, N] (B stacked matrices, e.g. experts; B = 1 for one
+ *          linear), row-major logical weights         in
+ *   w_nk : int8 [B, N, K]                               out
+ * K % 16 == 0 and N % 16 == 0 (the INT8 rules); the two buffers must not
+ * overlap (FQ_ERR_ARG).  Asynchronous on `stream`; the next kernel on the
+ * stream starts only after it has finished. */
+fq_status fq_repack_weight_kmajor_i8(const int8_t* w_kn, int64_t B, int64_t K, int64_t N, int8_t* w_nk,
+                                     fq_stream_t stream);
+
+/* The same repack for the einsum's E4M3 weights ([PR] item 3: the grouped
+ * einsum's weight operand), logical [G, D, N] -> stored [G, N, D].
+ *   w_gdn : E4M3 [G, D, N] in;  w_gnd : E4M3 [G, N, D] out.
+ * D % 128 == 0 and N % 128 == 0 (whole 128 x 128 scale blocks).  Block
+ * scales [G, D/128, N/128] keep their layout and need no repack. */
+fq_status fq_repack_weight_kmajor_fp8(const uint8_t* w_gdn, int64_t G, int64_t D, int64_t N, uint8_t* w_gnd,
+                                      fq_stream_t stream);
 
 /* ------------------------------------------------------------------ INT8 */
 
@@ -166,15 +195,22 @@ fq_status w8a8_quant_linear(const uint16_t* x, int64_t M, int64_t K,
  * provide the workspace w8a8_linear needs.  Same arguments and bit-identical
  * results as w8a8_linear, without the workspace.
  *   Scratch: a fixed ~10.5 MB array in device memory (16 KiB of arrival
- *   counters + 10 MiB of partial sums), reserved on every GPU that loads this
- *   library and held until the process exits.
+ *   counters + 10 MiB of partial sums).  The CUDA driver reserves it when it
+ *   loads this library's W8A8 module on a device - with lazy module loading
+ *   possibly inside the first call of any W8A8 entry point on that device -
+ *   and holds it until the process exits; every process that uses a W8A8
+ *   entry point pays for it, whether or not it calls this one.  If the device
+ *   has no room for it, that first call returns FQ_ERR_CUDA with an
+ *   out-of-memory code in fq_last_cuda_error().
  *   Limits: M <= 64, N <= 524288 (ceil(N/128) <= 4096 tiles), at most 160
  *   SMs; larger sizes return FQ_ERR_SHAPE (FQ_ERR_UNSUPPORTED_DEVICE for more
- *   SMs).  No cudaMalloc/cudaFree or allocating call is made.
+ *   SMs).  No cudaMalloc/cudaFree or allocating library call is made.
  *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture.  Each call zeroes the counters it uses with
- *   cudaMemsetAsync on `stream`, then launches the GEMM.
+ *   device, with that device current) and keeps it for the life of the
+ *   process; make that first call before any stream capture.  Resetting the
+ *   device (cudaDeviceReset, or a reset of its primary context) while the
+ *   library is loaded is not supported.  Each call zeroes the counters it
+ *   uses with cudaMemsetAsync on `stream`, then launches the GEMM.
  *   All calls share the one array: calls that may overlap on the GPU
  *   (different streams, or different host threads) race and give wrong
  *   results; serialise them. */

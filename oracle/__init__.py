@@ -23,8 +23,9 @@ Modules:
   norm    RMSNorm fused with the INT8 per-token or FP8 per-group quant.
   mx      32-element block-scaled FP8 (UE8M0 scale per block) and its linear.
   moe     sort-by-expert, gather, grouped W8A8, SwiGLU+requant, combine.
+  layout  load-time K-major weight repack.
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against values
 fixed by the pages, closed forms, invariants or brute force.
 """
-from . import codecs, int8, fp8, moe, norm, mx  # noqa: F401
+from . import codecs, int8, fp8, moe, norm, mx, layout  # noqa: F401

@@ -30,7 +30,8 @@ def test_header_declares_the_path():
     names = declared_functions()
     for n in ["dynamic_quant_int8", "quant_fp8_group_ue8m0_packed", "w8a8_linear", "w8a8_quant_linear",
               "fp8_group_einsum", "moe_sort", "w8a8_grouped_linear", "swiglu_quant_int8", "moe_combine",
-              "fq_workspace_bytes", "fq_status_string", "fq_device_error"]:
+              "fq_workspace_bytes", "fq_status_string", "fq_device_error", "fq_check_device_error",
+              "fq_repack_weight_kmajor_i8", "fq_repack_weight_kmajor_fp8"]:
         assert n in names, n
 
 
@@ -82,6 +83,12 @@ def test_host_validation_before_any_device_call(libfq):
     assert L.rmsnorm_quant_fp8_ue8m0_packed(None, None, 1e-6, 4, 4112, None, None, None) == 2
     assert L.rmsnorm_quant_int8(None, None, 1e-6, 0, 4096, None, None, None) == 0
     assert L.rmsnorm_quant_int8(None, None, 1e-6, 4, 4096, None, None, None) == 1
+    # load-time repack: divisibility, empty, null, overlapping buffers
+    assert L.fq_repack_weight_kmajor_i8(None, 1, 24, 16, None, None) == 2       # K % 16
+    assert L.fq_repack_weight_kmajor_fp8(None, 1, 128, 192, None, None) == 2    # N % 128
+    assert L.fq_repack_weight_kmajor_i8(None, 0, 16, 16, None, None) == 0       # empty
+    assert L.fq_repack_weight_kmajor_i8(None, 1, 16, 16, None, None) == 1
+    assert L.fq_repack_weight_kmajor_i8(ctypes.c_void_p(0x10000), 1, 64, 64, ctypes.c_void_p(0x10800), None) == 9
 
 
 def test_workspace_sizing_without_device_is_zero():
