@@ -1439,12 +1439,12 @@ __global__ void __launch_bounds__(um::kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-static int pick_mt(int64_t M) { return M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 32 ? 32 : 64)); }
+static constexpr int pick_mt(int64_t M) { return M <= 8 ? 8 : (M <= 16 ? 16 : (M <= 32 ? 32 : 64)); }
 
-static size_t slots_bytes(int sms, int mt) { return size_t(2) * sms * kBN * mt * 4; }
+static constexpr size_t slots_bytes(int sms, int mt) { return size_t(2) * sms * kBN * mt * 4; }
 // Token tile the partial-sum slots are sized for: the tcgen05 kernel runs
 // tiles of at least 32 tokens (a forced schedule may run it for any M).
-static int slots_mt(int64_t M) { return pick_mt(M) < 32 ? 32 : pick_mt(M); }
+static constexpr int slots_mt(int64_t M) { return pick_mt(M) < 32 ? 32 : pick_mt(M); }
 
 // Workspace layout: [counters: kCounterBytes][xq, sx: fused call only][partial-sum slots]
 size_t ws_w8a8_linear(int64_t M, int64_t K, int64_t N) {
@@ -1829,6 +1829,11 @@ constexpr int kMaxCtas = 160;                                    // one CTA per 
 constexpr size_t kCountersNA = size_t(kMaxTilesNA) * 4;         // 16 KiB of arrival counters
 constexpr size_t kSlotsNA = size_t(2) * kMaxCtas * kBN * 64 * 4;  // 10 MiB of int32 partial sums
 constexpr size_t kScratchBytes = kCountersNA + kSlotsNA;
+// the partial sums of every schedule a call within the limits can take (token
+// tiles up to 64, one CTA per SM), and one arrival counter per 128-row tile
+static_assert(kSlotsNA >= slots_bytes(kMaxCtas, slots_mt(kMaxM)), "partial-sum area too small");
+static_assert(size_t(kMaxTilesNA) * 4 <= kCountersNA, "counter area too small");
+static_assert(slots_mt(kMaxM) == kMaxM, "M <= kMaxM is one token tile on every schedule");
 }  // namespace noalloc
 
 // Held by every device that loads this library, for the life of the process.
