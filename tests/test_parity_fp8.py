@@ -262,3 +262,20 @@ def test_tiny_group_scale_byte_zero():
     assert torch.equal(yp.view(torch.int16), yf.view(torch.int16))
     want = of8.fp8_group_einsum(oxq, of8.unpack_scales(ost, T, D // 128), owq, osw)
     assert_within_tol(bf16_to_np(yp), want)
+
+
+def test_einsum_rows_independent_of_T():
+    """A token's output row does not depend on the other tokens of the call:
+    T = 1 and T = 3 give bit-for-bit the first rows of the T = 4 call on the
+    same inputs (the schedule depends on the token-tile count, which is the
+    same for all three, and each token's sums use only its own column)."""
+    G, D, N = 8, 4096, 1024
+    x4 = synth.group_activations(4, G, D, 7711)
+    _, _, wq, sw = einsum_weights(G, N, D, 7)
+    ys = {}
+    for T in (1, 3, 4):
+        xq, st = fq.quant_fp8_group_ue8m0_packed(bf16_to_dev(np.ascontiguousarray(x4[:T])))
+        ys[T] = fq.fp8_group_einsum(xq, st, fq.SCALE_UE8M0_PACKED, wq, sw).view(torch.int16)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[1], ys[4][:1])
+    assert torch.equal(ys[3], ys[4][:3])
