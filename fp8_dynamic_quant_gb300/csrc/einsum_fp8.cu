@@ -6,20 +6,29 @@
 //
 //   Y[t, g, n] = bf16( sum_kb sx[t,g,kb] * sw[g,kb,n/128] * sum_{d in kb} xq[t,g,d] * W[g,d,n] )
 //
-// GB300 design:
-//  * Swap-AB tiles of 128 weight rows (n) x MT tokens, one per (g, n-block,
-//    token tile); weights E4M3 [G, N, D] K-major, activations E4M3 [T, G, D].
-//  * Engine: warp-level e4m3 mma.sync (m16n8k32, fp32 accumulate), measured at
-//    ~2.3 PFLOP/s on GB300 - well above what decode-sized T needs to stay on
-//    the HBM roofline; no operand conversion is needed.  Each 128-wide K block
-//    (one scale block) is accumulated in fresh registers and then promoted:
-//    acc += blk * (sx * sw).  The scales of the next k-block are fetched while
-//    the current one computes.
-//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) producer warp + mbarrier
-//    ring + eight consumer warps, stream-K over (tile, k-block) iterations.
-//    Partial tiles are reduced by the last-arriving CTA in ascending CTA
+// GB300 design (5th-generation tensor cores, operands straight from TMA):
+//  * Swap-AB tiles: 128 weight rows (n; exactly one weight-scale block) x MT
+//    tokens (16, 32 or 64; more tokens take several token tiles), one tile per
+//    (g, n-block, token tile).  Weights E4M3 [G, N, D] K-major, activations
+//    E4M3 [T, G, D]; both land by TMA in the 128-byte-swizzled K-major layout
+//    the MMA reads, so nothing is converted.
+//  * warp 0 lane 0: TMA producer (weights of the first stages are issued at
+//    kernel entry, before the wait on the previous kernel);
+//  * warp 1: allocates tensor memory; lane 0 issues, per 128-wide K block,
+//    four tcgen05.mma kind::f8f6f4 (M = 128, N = MT, K = 32) into a fresh fp32
+//    accumulator slot in tensor memory, and commits once per group of four K
+//    blocks (a commit costs about a tensor-pipe drain): two groups of slots
+//    alternate;
+//  * warps 2..5: one weight row per thread.  Per group they wait once, then
+//    per K block drain its slot (tcgen05.ld) and promote it into fp32
+//    registers: acc += blk * (sx[t] * sw) - the per-128-K block scaling.  The
+//    scales stream in a few blocks ahead by asynchronous copies.
+//  * Stream-K over the flattened (tile, K block) range, one CTA per SM: the
+//    partial tiles at a CTA's range ends go to workspace slots and the last
+//    CTA to finish a tile adds every contributor's slot in ascending CTA
 //    order, so the fp32 result does not depend on timing: the packed-scale
-//    and fp32-scale calls produce identical bits.
+//    and fp32-scale calls produce identical bits, and a token's row does not
+//    depend on the other tokens of the call.
 //  * The scale format only changes how sx is decoded: packed byte
 //    ((g*P + kb/4)*Ta + t)*4 + kb%4 -> 2^(u-127), or the fp32 value.
 #include <cstdlib>
@@ -32,33 +41,65 @@ namespace fq {
 namespace es {
 constexpr int kBK = 128;
 constexpr int kMaxGrid = 1024;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kPre = 4;  // K blocks of scales in flight ahead of the promotion
+// K blocks per tensor-core commit.  A tcgen05.commit costs about a pipeline
+// drain (~0.3 us measured on GB300 for decode-sized MMAs, against ~25 ns per
+// 128x16x32 MMA when they stream), so stage release and the accumulator
+// hand-off are signalled once per group of K blocks; a group also ends at
+// every stream-K segment end and at the end of the CTA's range.
+constexpr int kGroupBars = 24;  // ring of group-completion barriers (more than the stages)
+// Blocks per commit group (two groups of MT-column slots in tensor memory).
+template <int MT>
+struct GroupSize {
+  static constexpr int value = 4;
+};
 
-// MT tokens per tile, CW consumer warps of 16 weight rows (BN = 16 * CW, a
-// divisor of the 128-wide weight-scale block), one producer warp.
-template <int MT, int CW>
+// Walks a CTA's (tile, K block) iterations and their commit groups; every
+// role keeps one, so they agree on the group boundaries.
+template <int GROUP>
+struct GroupCursor {
+  int r = 0, kb = 0, g = 0, cnt = 0;
+  // is iteration r the last of its group?
+  __device__ __forceinline__ bool group_end(int KB, int n_it) const {
+    return cnt + 1 == GROUP || kb == KB - 1 || r == n_it - 1;
+  }
+  __device__ __forceinline__ void advance(int KB, int n_it) {
+    if (group_end(KB, n_it)) {
+      ++g;
+      cnt = 0;
+    } else {
+      ++cnt;
+    }
+    if (++kb == KB) kb = 0;
+    ++r;
+  }
+};
+
+template <int MT>
 struct Cfg {
-  static constexpr int NT = MT / 8;
-  static constexpr int BN = 16 * CW;
-  static constexpr int THREADS = (CW + 1) * 32;
-  static constexpr int W_BYTES = BN * kBK;
+  static constexpr int W_BYTES = 128 * kBK;
   static constexpr int X_BYTES = MT * kBK;
   static constexpr int STAGE = W_BYTES + X_BYTES;  // multiple of 1024
-  static constexpr int EPI = BN * MT * 2;
-  static constexpr int SCALES = (MT + 4) * 4;      // per stage: MT token scale words + sw
-  // ~200 KB of weights in flight per SM to cover loaded HBM latency
-  static constexpr int STAGES_FIT = (212 * 1024 - EPI - 4096) / (STAGE + SCALES);
-  static constexpr int STAGES = STAGES_FIT > 24 ? 24 : STAGES_FIT;
-  static constexpr int SLOT = BN * MT;             // fp32 per slot
-  static constexpr int SMEM = STAGES * STAGE + EPI + STAGES * SCALES + 2 * STAGES * 8 + 64 + 1024;
-  static_assert(STAGES >= 3, "pipeline too shallow");
-  static_assert(128 % BN == 0, "tile must sit inside one weight-scale block");
+  // ~200 KB of weights in flight per SM to cover loaded HBM latency (half
+  // that, to fit two CTAs per SM, measured slower: 17.5 against 15 us at T=1)
+  static constexpr int STAGES_FIT = (208 * 1024) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
+  static constexpr int GROUP = GroupSize<MT>::value;
+  static constexpr int NACC = 2 * GROUP;           // accumulator slots: two groups of K blocks
+  static constexpr uint32_t TMEM_COLS = NACC * MT <= 128 ? 128u : (NACC * MT <= 256 ? 256u : 512u);
+  static constexpr int SLOT = 128 * MT;             // fp32 per partial-sum slot
+  static constexpr int SMEM = STAGES * STAGE + (STAGES + kGroupBars + 2 + 1) * 8 + 1024;
+  static_assert(STAGES >= 4, "pipeline too shallow");
+  static_assert(NACC * MT <= 512, "tensor-memory budget");
+  static_assert(kGroupBars > STAGES, "group barriers must outnumber the stages (no parity aliasing)");
 };
 
 struct Problem {
   int T, G, D, N, KB, NB, TT, P, Ta;
   int64_t total;
   const void* sx;
-  int fmt;
   const float* sw;
   uint16_t* y;
   float* slots;
@@ -66,67 +107,19 @@ struct Problem {
   uint32_t* err;
 };
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ void mma_e4m3(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int s) {
-  return s == 0 ? v.x : (s == 1 ? v.y : (s == 2 ? v.z : v.w));
-}
-
-// 4-byte asynchronous copy global -> shared (completion tracked by the
-// executing thread's cp.async group, announced on an mbarrier below).
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (no pending-count increment: the barrier's count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Decoded activation scale from its stored word: a packed UE8M0 word holds
-// four k-blocks' exponent bytes, byte u meaning 2^(u-127) (u = 0 is the
-// subnormal 2^-127, kept exact so both formats give identical bits); an fp32
-// word is the scale itself.  `sel` picks byte kb % 4, zero-extended.
-template <int FMT>
-__device__ __forceinline__ float decode_sx(uint32_t w, uint32_t sel) {
-  if (FMT == FQ_SCALE_UE8M0_PACKED) {
-    const uint32_t u = __byte_perm(w, 0u, sel);
-    return __uint_as_float(u ? (u << 23) : 0x00400000u);
-  }
-  return __uint_as_float(w);
-}
-
-// Fragment row g (0..7) of a 16-row block reads shared-memory row R(g), so the
-// two rows of each quarter-warp phase of a 16-byte ld.shared fall in different
-// halves of the 128-byte swizzle atom (conflict-free).
-__device__ __forceinline__ int frag_row(int g) { return (g >> 1) | ((g & 1) << 2); }
-
-// CTA whose stream-K range holds iteration i: the largest c with rb[c] <= i.
-__device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
+// First iteration of CTA c's stream-K range: floor(c * total / G).
+__device__ __forceinline__ int range_begin(int64_t total, int G, int c) { return int(int64_t(c) * total / G); }
+// CTA whose stream-K range holds iteration i: the largest c with range_begin(c) <= i.
+__device__ __forceinline__ int cta_of(int64_t total, int G, int i) {
   int lo = 0, hi = G;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (rb[mid] <= i) lo = mid; else hi = mid;
+    if (range_begin(total, G, mid) <= i) lo = mid; else hi = mid;
   }
   return lo;
 }
 
-// tile = (g * NB + nb) * TT + tt, NB = N / BN
+// tile = (g * NB + nb) * TT + tt
 struct ETile {
   int g, nb, tt;
 };
@@ -139,281 +132,367 @@ __device__ __forceinline__ ETile etile(const Problem& p, int tile) {
   return t;
 }
 
-template <int MT, int CW, int FMT>
-__global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
+// Activation scale of K block kb from its stored word: a packed UE8M0 word
+// holds four K blocks' exponent bytes, byte u meaning 2^(u-127) (u = 0 is the
+// subnormal 2^-127, kept exact so both formats give identical bits); an fp32
+// word is the scale itself.
+template <int FMT>
+__device__ __forceinline__ float decode_sx(uint32_t w, int kb) {
+  if (FMT == FQ_SCALE_UE8M0_PACKED) {
+    const uint32_t u = (w >> (8 * (kb & 3))) & 0xFFu;
+    return __uint_as_float(u ? (u << 23) : 0x00400000u);
+  }
+  return __uint_as_float(w);
+}
+
+// 4-byte asynchronous copy global -> shared, tracked by the issuing thread's
+// commit groups.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4 (E4M3 x E4M3 -> fp32), one thread.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::f8f6f4: fp32 accumulator (bits 4-5 = 1),
+// A and B E4M3 (format 0) and K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N) {
+  return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+template <int MT, int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
     fp8_einsum_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
-  using C = Cfg<MT, CW>;
-  constexpr int NT = C::NT, S = C::STAGES, BN = C::BN, kCW = CW, kThreads = C::THREADS;
+  using C = Cfg<MT>;
+  constexpr int S = C::STAGES, NACC = C::NACC, kEpi = kEpiWarps * 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = smem;
-  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + S * C::STAGE);
-  uint32_t* scl = reinterpret_cast<uint32_t*>(smem + S * C::STAGE + C::EPI);  // [S][MT + 4]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE + C::EPI + S * C::SCALES);
-  uint64_t* empty = full + S;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE);
+  uint64_t* grp = full + S;                 // [kGroupBars]: the MMAs of group g have completed
+  uint64_t* acc_empty = grp + kGroupBars;   // [2]: the epilogue has drained group g's slots
+  uint64_t* done_bar = acc_empty + 2;
+  __shared__ uint32_t s_tmem;
   __shared__ int s_flag, s_issued, s_consumed;
   __shared__ volatile int s_abort;
-  __shared__ int rb[kMaxGrid + 1];
+  __shared__ __align__(16) float s_f[kEpiWarps][MT];        // per-token scale factors of the current block
+  __shared__ __align__(16) uint32_t s_ring[kEpiWarps][kPre * (MT + 4)];  // scale words, kPre blocks ahead
+  __shared__ __align__(16) uint16_t s_ystage[16 * 128];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, b = blockIdx.x;
+  int npre = 0;
   if (tid == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1 + 32);  // producer's expect-tx arrival + 32 scale-copy arrivals
-      mbar_init(&empty[i], kCW);
-    }
+    for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kGroupBars; ++i) mbar_init(&grp[i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&acc_empty[i], kEpiWarps);
+    mbar_init(done_bar, 1);
     fence_barrier_init();
     s_issued = 0;
     s_consumed = 0;
     s_abort = 0;
-  }
-  if (warp == kCW && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    // weights do not depend on the previous kernel: the first stages go out now
+    const int b0 = int(int64_t(b) * p.total / G), b1 = int(int64_t(b + 1) * p.total / G);
+    npre = min(b1 - b0, S);
+    const uint64_t pol_w = p.TT > 1 ? policy_evict_normal() : policy_evict_first();
+    int tile = b0 / p.KB, kb = b0 - tile * p.KB;
+    ETile t = etile(p, tile);
+    for (int r = 0; r < npre; ++r) {
+      mbar_arrive_expect_tx(&full[r], C::STAGE);
+      tma_load_2d(smem + r * C::STAGE, &tmW, &full[r], kb * kBK, t.g * p.N + t.nb * 128, pol_w);
+      if (++kb == p.KB && r + 1 < npre) {
+        kb = 0;
+        t = etile(p, ++tile);
+      }
+    }
   }
-  const int G = gridDim.x, b = blockIdx.x;
-  for (int c = tid; c <= G; c += kThreads) rb[c] = int(int64_t(c) * p.total / G);
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  const int begin = rb[b], end = rb[b + 1];
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int begin = range_begin(p.total, G, b), end = range_begin(p.total, G, b + 1), n_it = end - begin;
   const int KB = p.KB;
-  const int NB128 = p.N / 128;
 
-  if (warp == kCW) {
-    // ------------------------------------------------ producer warp (all lanes)
-    if (end > begin) {
-      // weights streamed once (one token tile): evict-first; else keep for reuse
+  if (warp == 0) {
+    // ------------------------------------------------ producer
+    if (lane == 0 && n_it > 0) {
       const uint64_t pol_w = p.TT > 1 ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const int n_it = end - begin;
-      const int npre = n_it < S ? n_it : S;
-      if (lane == 0) {  // weights do not depend on the previous kernel: issue them first
-        int tile = begin / KB, kb = begin - tile * KB;
-        ETile t = etile(p, tile);
-        for (int r = 0; r < npre; ++r) {
-          mbar_arrive_expect_tx(&full[r], C::STAGE);
-          tma_load_2d(stages + r * C::STAGE, &tmW, &full[r], kb * kBK, t.g * p.N + t.nb * BN, pol_w);
-          if (++kb == KB && r + 1 < npre) {
-            kb = 0;
-            t = etile(p, ++tile);
-          }
-        }
-      }
       pdl_wait();
       int tile = begin / KB, kb = begin - tile * KB;
       ETile t = etile(p, tile);
       int issued = 0;
+      GroupCursor<C::GROUP> lag;  // the iteration that last used the stage being refilled
+      lag.kb = kb;
       for (int r = 0; r < n_it; ++r) {
         const int s = r % S;
+        uint8_t* st = smem + s * C::STAGE;
         if (r >= npre) {
-          int ok = 1;
-          if (lane == 0) ok = (!s_abort && mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) ? 1 : 0;
-          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-          if (!ok) {
-            if (lane == 0) {
-              if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
-              s_abort = 1;
-            }
+          // stage s held iteration r - S: wait until that iteration's group completed
+          const int gl = lag.g;
+          lag.advance(KB, n_it);
+          if (s_abort || !mbar_wait(&grp[gl % kGroupBars], uint32_t((gl / kGroupBars) & 1))) {
+            if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+            s_abort = 1;
             break;
           }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&full[s], C::STAGE);
-            tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], kb * kBK, t.g * p.N + t.nb * BN, pol_w);
-          }
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(st, &tmW, &full[s], kb * kBK, t.g * p.N + t.nb * 128, pol_w);
         }
-        if (lane == 0)
-          tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
-        // this stage's token scale words and the tile's weight-block scale
-        uint32_t* sc = scl + s * (MT + 4);
-        if (lane == 0) cp_async4(sc + MT, p.sw + (int64_t(t.g) * KB + kb) * NB128 + (t.nb * BN) / 128);
-        if (FMT == FQ_SCALE_UE8M0_PACKED) {
-          // packed words of 4 consecutive tokens are contiguous and 16-byte
-          // aligned (the token dimension is padded to a multiple of 4)
-          for (int c4 = lane; c4 < MT / 4; c4 += 32) {
-            const int tok0 = t.tt * MT + 4 * c4;
-            if (tok0 < p.Ta)
-              cp_async16(sc + 4 * c4,
-                         static_cast<const int32_t*>(p.sx) + (int64_t(t.g) * p.P + (kb >> 2)) * p.Ta + tok0);
-          }
-        } else {
-          for (int m = lane; m < MT; m += 32) {
-            const int tok = t.tt * MT + m;
-            if (tok < p.T)  // tokens past T are not copied; consumers use 0 for them
-              cp_async4(sc + m, static_cast<const float*>(p.sx) + (int64_t(tok) * p.G + t.g) * KB + kb);
-          }
-        }
-        cp_async_arrive_noinc(&full[s]);
+        tma_load_2d(st + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
         ++issued;
         if (++kb == KB && r + 1 < n_it) {
           kb = 0;
           t = etile(p, ++tile);
         }
       }
-      if (lane == 0) s_issued = issued;
+      s_issued = issued;
     }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // The issuing thread's own instruction stream is on the critical path
+      // (one thread, dependent integer work between MMAs), so descriptors are
+      // formed once and advanced by adding the address offset (in 16-byte
+      // units) to their low field, and the stage / phase counters step
+      // incrementally.
+      const uint64_t da0 = umma_desc_k_sw128(smem_u32(smem));
+      const uint64_t db0 = umma_desc_k_sw128(smem_u32(smem) + C::W_BYTES);
+      constexpr uint32_t idesc = idesc_f8(128, MT);
+      int consumed = 0, s = 0;
+      uint32_t phase = 0;
+      GroupCursor<C::GROUP> cur;
+      cur.kb = begin % KB;
+      for (int r = 0; r < n_it; ++r) {
+        bool ok = !s_abort;
+        // a group reuses the slots of the group two back: wait until the epilogue drained it
+        if (ok && cur.cnt == 0 && cur.g >= 2)
+          ok = mbar_wait(&acc_empty[cur.g & 1], uint32_t(((cur.g >> 1) - 1) & 1));
+        if (ok) ok = mbar_wait(&full[s], phase);
+        if (!ok) {
+          if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
+          s_abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t off = uint64_t(uint32_t(s * C::STAGE) >> 4);
+        const uint32_t d = tmem + uint32_t(((cur.g & 1) * C::GROUP + cur.cnt) * MT);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) umma_f8(d, da0 + off + uint64_t(2 * j), db0 + off + uint64_t(2 * j), idesc, j > 0 ? 1u : 0u);
+        // one commit per group: releases the group's stages and hands its slots to the epilogue
+        if (cur.group_end(KB, n_it)) umma_commit(&grp[cur.g % kGroupBars]);
+        cur.advance(KB, n_it);
+        ++consumed;
+        if (++s == S) {
+          s = 0;
+          phase ^= 1u;
+        }
+      }
+      umma_commit(done_bar);
+      if (!mbar_wait(done_bar, 0)) atomicOr(p.err, DEVERR_TIMEOUT);
+      s_consumed = consumed;  // stages whose copies are known to have landed
+    }
+    __syncwarp();
   } else {
+    // ------------------------------------------------ promotion + epilogue
     pdl_wait();
     // Let the next kernel launch only once this one's inputs are final: a
     // dependent may prefetch weights before its own wait, which is safe only
     // if every earlier kernel has finished.
     pdl_launch_dependents();
-    const int gq = lane >> 2, c = lane & 3;
-    const int rg = frag_row(gq);
-    float acc[NT][4];
+    const int q = warp & 3, nl = 32 * q + lane, etid = tid - 64;
+    const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
+    float* sf = s_f[warp - 2];
+    float acc[MT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[j][r] = 0.f;
-    const uint32_t sbase = smem_u32(stages);
-    const uint32_t rowW0 = uint32_t((16 * warp + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
-    int tile = begin / KB, kb = begin - tile * KB;
+    for (int j = 0; j < MT; ++j) acc[j] = 0.0f;
+    int tile = begin / KB, kb = begin - tile * KB, seg_kb0 = kb;
     ETile t = etile(p, tile);
-    int seg_kb0 = kb;
     bool first_seg = true;
-    int consumed = 0;
-    const int n_it = end - begin;
-    for (int r = 0; r < n_it; ++r) {
-      const int s = r % S;
-      bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
-      if (!ok) {
-        if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
-        s_abort = 1;
+    // Scales stream through a per-warp ring in shared memory, kPre blocks
+    // ahead, by asynchronous 4-byte copies (lane j copies token j's stored
+    // word, and j + 32's; lane 0 the weight-block scale): a block's promotion
+    // never waits on a global round trip.  Slot layout: MT token words, then sw.
+    constexpr int TPL = MT > 32 ? 2 : 1;
+    uint32_t* ring = s_ring[warp - 2];
+    int tile_p = tile, kb_p = kb;  // block of the next copy to issue
+    auto issue = [&](int it) {
+      const ETile tp = etile(p, tile_p);
+      uint32_t* slot = ring + (it % kPre) * (MT + 4);
+#pragma unroll
+      for (int i = 0; i < TPL; ++i) {
+        const int m = lane + 32 * i, tok = tp.tt * MT + m;
+        if (m < MT && tok < p.T) {
+          const void* src = FMT == FQ_SCALE_UE8M0_PACKED
+                                ? static_cast<const void*>(static_cast<const uint32_t*>(p.sx) +
+                                                           (int64_t(tp.g) * p.P + (kb_p >> 2)) * p.Ta + tok)
+                                : static_cast<const void*>(static_cast<const float*>(p.sx) +
+                                                           (int64_t(tok) * p.G + tp.g) * KB + kb_p);
+          cp_async4(slot + m, src);
+        }
       }
+      if (lane == 0) cp_async4(slot + MT, p.sw + (int64_t(tp.g) * KB + kb_p) * p.NB + tp.nb);
+      if (++kb_p == KB) {
+        kb_p = 0;
+        ++tile_p;
+      }
+    };
+#pragma unroll 1
+    for (int it = 0; it < kPre; ++it) {
+      if (it < n_it) issue(it);
+      cp_async_commit();
+    }
+    GroupCursor<C::GROUP> ec;
+    ec.kb = kb;
+    bool gok = true;
+    for (int r = 0; r < n_it; ++r) {
+      const bool seg_end = (kb == KB - 1) || (r == n_it - 1);
+      // this block's per-token factors sx[t] * sw (0 past T), through shared memory
+      cp_async_wait<kPre - 1>();
+      __syncwarp();
+      {
+        const uint32_t* slot = ring + (r % kPre) * (MT + 4);
+        const float swv = __uint_as_float(slot[MT]);
+        float fv[TPL];
+#pragma unroll
+        for (int i = 0; i < TPL; ++i) {
+          const int m = lane + 32 * i;
+          fv[i] = (m < MT && t.tt * MT + m < p.T) ? __fmul_rn(decode_sx<FMT>(slot[m], kb), swv) : 0.0f;
+        }
+        __syncwarp();  // the slot is read; its next copy may go out
+#pragma unroll
+        for (int i = 0; i < TPL; ++i)
+          if (lane + 32 * i < MT) sf[lane + 32 * i] = fv[i];
+      }
+      if (r + kPre < n_it) issue(r + kPre);
+      cp_async_commit();
+      __syncwarp();
+      if (ec.cnt == 0) {  // a group starts: wait once for all of its MMAs
+        gok = !s_abort && mbar_wait(&grp[ec.g % kGroupBars], uint32_t((ec.g / kGroupBars) & 1));
+        gok = __all_sync(0xFFFFFFFFu, gok);
+        if (!gok) {
+          if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+          s_abort = 1;
+        }
+        tc_fence_after();
+      }
+      const bool ok = gok;
+      const uint32_t acol = uint32_t(((ec.g & 1) * C::GROUP + ec.cnt) * MT);
       if (ok) {
-        const uint32_t st = sbase + uint32_t(s * C::STAGE);
-        // one fp32 chain per 64-byte half when there are few token tiles
-        constexpr int NB2 = NT <= 2 ? 2 : 1;
-        float blk[NB2][NT][4];
+        // 16 columns at a time: load, wait, promote (keeps the registers of
+        // one chunk, not of the whole tile, in flight)
 #pragma unroll
-        for (int a = 0; a < NB2; ++a)
+        for (int h = 0; h < MT / 16; ++h) {
+          uint32_t v[16];
+          tmem_ld16(trow + acol + uint32_t(16 * h), v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) blk[a][j][rr] = 0.f;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
-          const uint4 wa = lds128(st + rowW0 + q);
-          const uint4 wb = lds128(st + rowW1 + q);
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const uint4 xv = lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q);
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks)
-              mma_e4m3(blk[h % NB2][j], word_of(wa, 2 * ks), word_of(wb, 2 * ks), word_of(wa, 2 * ks + 1),
-                       word_of(wb, 2 * ks + 1), word_of(xv, 2 * ks), word_of(xv, 2 * ks + 1));
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 f = *reinterpret_cast<const float4*>(sf + 16 * h + 4 * j4);
+            float* a4 = acc + 16 * h + 4 * j4;
+            a4[0] = __fmaf_rn(__uint_as_float(v[4 * j4 + 0]), f.x, a4[0]);
+            a4[1] = __fmaf_rn(__uint_as_float(v[4 * j4 + 1]), f.y, a4[1]);
+            a4[2] = __fmaf_rn(__uint_as_float(v[4 * j4 + 2]), f.z, a4[2]);
+            a4[3] = __fmaf_rn(__uint_as_float(v[4 * j4 + 3]), f.w, a4[3]);
           }
         }
-        const uint32_t* sc = scl + s * (MT + 4);
-        const float swv = __uint_as_float(sc[MT]);
-        const uint32_t sel = 0x4440u | uint32_t(kb & 3);  // byte kb % 4 of the word, zero-extended
-        float sxs[NT][2];
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int ml = 8 * j + frag_row(2 * c + hh);
-            sxs[j][hh] = (t.tt * MT + ml < p.T) ? decode_sx<FMT>(sc[ml], sel) : 0.f;
-          }
-        // The stage was read through the generic proxy (ld.shared); the next
-        // TMA write into it goes through the async proxy.  Order the two
-        // before handing the stage back, or TMA can overwrite it under the read.
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        ++consumed;
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            const float bsum = NB2 == 2 ? __fadd_rn(blk[0][j][rr], blk[NB2 - 1][j][rr]) : blk[0][j][rr];
-            acc[j][rr] = __fmaf_rn(bsum, __fmul_rn(sxs[j][rr & 1], swv), acc[j][rr]);
-          }
       }
-      if (kb == KB - 1 || r == n_it - 1) {
+      tc_fence_before();
+      __syncwarp();
+      // the group's last block is read: its slots may take the group after next
+      if (ec.group_end(KB, n_it) && lane == 0 && ok) mbar_arrive(&acc_empty[ec.g & 1]);
+      ec.advance(KB, n_it);
+      __syncwarp();  // sf is rewritten for the next block
+      if (seg_end) {
+        // ---- segment end: tile `tile`, K blocks [seg_kb0, kb]
+        const int n0 = t.nb * 128, m0 = t.tt * MT;
+        const int rows = min(MT, p.T - m0);
         const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
-        bool do_epi = whole;
         if (!whole) {
-          float* my = p.slots + (2 * b + (first_seg ? 0 : 1)) * int64_t(C::SLOT);
+          // this CTA's partial sums -> its slot [MT tokens][128 rows]
+          float* my = p.slots + (2 * int64_t(b) + (first_seg ? 0 : 1)) * C::SLOT + nl;
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) my[((warp * NT + j) * 4 + rr) * 32 + lane] = acc[j][rr];
-          named_bar_sync(1, kCW * 32);
-          if (tid == 0) {
+          for (int j = 0; j < MT; ++j) my[j * 128] = acc[j];
+          named_bar_sync(1, kEpi);
+          if (etid == 0) {
             const uint32_t nbk = uint32_t(kb - seg_kb0 + 1);
             const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile], nbk);
             const int last = (old + nbk == uint32_t(KB)) ? 1 : 0;
-            if (last) p.counters[tile] = 0;
+            if (last) p.counters[tile] = 0;  // every contributor has arrived; ready for the next call
             s_flag = last;
           }
-          named_bar_sync(1, kCW * 32);
-          do_epi = s_flag != 0;
-          if (do_epi) {
-            // Fixed order: ascending CTA index over every contributor's slot
-            // (this CTA's own partial included, read back from its slot), so
-            // the fp32 sum does not depend on which CTA arrives last.
-            constexpr int U = NT <= 2 ? 8 : (NT <= 4 ? 4 : 2);
-            const int c0 = cta_of(rb, G, tile * KB), c1 = cta_of(rb, G, tile * KB + KB - 1);
-            float tot[NT][4];
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-              for (int rr = 0; rr < 4; ++rr) tot[j][rr] = 0.f;
-            for (int cb = c0; cb <= c1; cb += U) {
-              float v[U][NT][4];
-              bool use[U];
-#pragma unroll
-              for (int u = 0; u < U; ++u) {
-                const int cc = cb + u;
-                use[u] = cc <= c1 && rb[cc + 1] != rb[cc];
-                const int first_tile = use[u] ? rb[cc] / KB : 0;
-                const float* sl = p.slots + (2 * int64_t(cc) + (first_tile == tile ? 0 : 1)) * int64_t(C::SLOT);
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                  for (int rr = 0; rr < 4; ++rr)
-                    v[u][j][rr] = use[u] ? __ldcg(sl + ((warp * NT + j) * 4 + rr) * 32 + lane) : 0.f;
-              }
-#pragma unroll
-              for (int u = 0; u < U; ++u)
-                if (use[u]) {
-#pragma unroll
-                  for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) tot[j][rr] = __fadd_rn(tot[j][rr], v[u][j][rr]);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-              for (int rr = 0; rr < 4; ++rr) acc[j][rr] = tot[j][rr];
-          }
-          named_bar_sync(1, kCW * 32);  // s_flag is rewritten by the next segment
+          named_bar_sync(1, kEpi);
         }
+        const bool do_epi = whole || s_flag != 0;
         if (do_epi) {
+          if (!whole) {
+            // every contributor's slot, this CTA's own included, added in
+            // ascending CTA order; four contributors' loads in flight at once
+            const int c0 = cta_of(p.total, G, tile * KB), c1 = cta_of(p.total, G, tile * KB + KB - 1);
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
+            for (int j = 0; j < MT; ++j) acc[j] = 0.0f;
+            for (int cb = c0; cb <= c1; cb += 4) {
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-              const int nl = 16 * warp + rg + ((rr & 2) ? 8 : 0);
-              const int ml = 8 * j + frag_row(2 * c + (rr & 1));
-              epi[ml * BN + nl] = f32_to_bf16_bits(acc[j][rr]);
-            }
-          named_bar_sync(1, kCW * 32);
-          const int n0 = t.nb * BN;
-          for (int idx = tid; idx < MT * (BN / 8); idx += kCW * 32) {
-            const int ml = idx / (BN / 8), c8 = idx % (BN / 8);
-            const int tok = t.tt * MT + ml;
-            if (tok < p.T) {
-              const uint4 v = *reinterpret_cast<const uint4*>(epi + ml * BN + c8 * 8);
-              *reinterpret_cast<uint4*>(p.y + (int64_t(tok) * p.G + t.g) * p.N + n0 + c8 * 8) = v;
+              for (int h = 0; h < MT / 16; ++h) {
+                float vv[4][16];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int cc = cb + u;
+                  const int cb0 = range_begin(p.total, G, cc);
+                  const bool use = cc <= c1 && range_begin(p.total, G, cc + 1) != cb0;
+                  const int first_tile = use ? cb0 / KB : tile;
+                  const float* sl = p.slots + (2 * int64_t(use ? cc : b) + (first_tile == tile ? 0 : 1)) * C::SLOT +
+                                    nl + 16 * h * 128;
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) vv[u][j] = use ? __ldcg(sl + j * 128) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (cb + u <= c1 && range_begin(p.total, G, cb + u + 1) != range_begin(p.total, G, cb + u)) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[16 * h + j] = __fadd_rn(acc[16 * h + j], vv[u][j]);
+                  }
+              }
             }
           }
-          named_bar_sync(1, kCW * 32);
+          // bf16 through a staging tile, 16 tokens at a time, 16-byte stores
+#pragma unroll
+          for (int h = 0; h < MT / 16; ++h) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s_ystage[j * 128 + nl] = f32_to_bf16_bits(acc[16 * h + j]);
+            named_bar_sync(1, kEpi);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int piece = i * kEpi + etid, j = piece >> 4, c8 = piece & 15;
+              const int m = 16 * h + j;
+              if (m < rows)
+                st_global_v4(p.y + (int64_t(m0 + m) * p.G + t.g) * p.N + n0 + 8 * c8,
+                             *reinterpret_cast<const uint4*>(&s_ystage[j * 128 + 8 * c8]));
+            }
+            named_bar_sync(1, kEpi);
+          }
         }
+        if (!whole) named_bar_sync(1, kEpi);  // s_flag is rewritten by the next segment
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) acc[j][rr] = 0.f;
+        for (int j = 0; j < MT; ++j) acc[j] = 0.0f;
         first_seg = false;
         seg_kb0 = 0;
       }
@@ -422,21 +501,24 @@ __global__ void __launch_bounds__(Cfg<MT, CW>::THREADS, 1)
         t = etile(p, ++tile);
       }
     }
-    if (tid == 0) s_consumed = consumed;
   }
   __syncthreads();
   if (tid == 0) {
     for (int r = s_consumed; r < s_issued; ++r) mbar_wait(&full[r % S], uint32_t((r / S) & 1));
   }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
 }
 
-int pick_mt(int64_t T) { return T <= 8 ? 8 : (T <= 16 ? 16 : (T <= 32 ? 32 : 64)); }
+int pick_mt(int64_t T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
 
-template <int MT, int CW, int FMT>
+template <int MT, int FMT>
 cudaError_t launch_es1(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid, cudaStream_t s,
                        bool pdl) {
-  using Cf = Cfg<MT, CW>;
-  auto k = fp8_einsum_kernel<MT, CW, FMT>;
+  using Cf = Cfg<MT>;
+  auto k = fp8_einsum_kernel<MT, FMT>;
   static uint64_t attr_done = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -445,14 +527,14 @@ cudaError_t launch_es1(const CUtensorMap* tw, const CUtensorMap* tx, const Probl
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << (dev & 63);
   }
-  return launch(k, dim3(grid), dim3(Cf::THREADS), size_t(Cf::SMEM), s, pdl, *tw, *tx, p);
+  return launch(k, dim3(grid), dim3(kThreads), size_t(Cf::SMEM), s, pdl, *tw, *tx, p);
 }
 // The scale format is a compile-time parameter of the kernel.
-template <int MT, int CW>
-cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid, cudaStream_t s,
-                      bool pdl) {
-  return p.fmt == FQ_SCALE_UE8M0_PACKED ? launch_es1<MT, CW, FQ_SCALE_UE8M0_PACKED>(tw, tx, p, grid, s, pdl)
-                                        : launch_es1<MT, CW, FQ_SCALE_FP32>(tw, tx, p, grid, s, pdl);
+template <int MT>
+cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int fmt, int grid,
+                      cudaStream_t s, bool pdl) {
+  return fmt == FQ_SCALE_UE8M0_PACKED ? launch_es1<MT, FQ_SCALE_UE8M0_PACKED>(tw, tx, p, grid, s, pdl)
+                                      : launch_es1<MT, FQ_SCALE_FP32>(tw, tx, p, grid, s, pdl);
 }
 }  // namespace es
 
@@ -484,64 +566,51 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(T) * G * N * 2, s));
   const int mt = es::pick_mt(T);
-  const int64_t TT = (T + mt - 1) / mt;
-  // Schedule: 128-row tiles split stream-K over one CTA per SM.  The other
-  // schedule - 64-row tiles, one whole tile per CTA - measured slower on GB300
-  // at every decode size (T = 1..256) and is only taken when forced.
-  const int64_t tiles64 = G * (N / 64) * TT;
-  bool data_parallel = false;
-  // FQ_FORCE_SCHEDULE = dp | streamk overrides the choice (tests and studies)
-  if (const char* f = std::getenv("FQ_FORCE_SCHEDULE")) {
-    if (!std::strcmp(f, "dp") && tiles64 <= es::kMaxGrid) data_parallel = true;
-    if (!std::strcmp(f, "streamk")) data_parallel = false;
-  }
-  const int bn = data_parallel ? 64 : 128;
   es::Problem p = {};
   p.T = int(T);
   p.G = int(G);
   p.D = int(D);
   p.N = int(N);
   p.KB = int(D / 128);
-  p.NB = int(N / bn);
-  p.TT = int(TT);
+  p.NB = int(N / 128);
+  p.TT = int((T + mt - 1) / mt);
   p.P = int((D / 128 + 3) / 4);
   p.Ta = int((T + 3) / 4 * 4);
-  const int64_t tiles = G * p.NB * TT;
+  const int64_t tiles = G * p.NB * int64_t(p.TT);
   if (tiles > kMaxTiles || tiles * p.KB > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
   p.total = tiles * p.KB;
   const size_t need = kCounterBytes + size_t(2) * d.sm_count * 128 * mt * 4;
   if (!ws || ws_bytes < need) return FQ_ERR_WORKSPACE;
   if (!aligned16(ws)) return FQ_ERR_ALIGN;
   p.sx = sx;
-  p.fmt = fmt;
   p.sw = sw_blk;
   p.y = y;
   p.counters = static_cast<uint32_t*>(ws);
   p.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
   p.err = d.err_word;
   CUtensorMap tw_map, tx_map;
-  if (!tensor_map_u8_2d(&tw_map, w_gnd, uint64_t(D), uint64_t(G * N), uint64_t(D), es::kBK, uint32_t(bn)) ||
+  if (!tensor_map_u8_2d(&tw_map, w_gnd, uint64_t(D), uint64_t(G * N), uint64_t(D), es::kBK, 128u) ||
       !tensor_map_u8_2d(&tx_map, xq, uint64_t(G * D), uint64_t(T), uint64_t(G * D), es::kBK, uint32_t(mt)))
     return FQ_ERR_CUDA;
-  const CUtensorMap* tw = &tw_map;
-  const CUtensorMap* tx = &tx_map;
-  const int grid = data_parallel ? int(tiles) : int(p.total < d.sm_count ? p.total : d.sm_count);
+  // Schedule: stream-K over one CTA per SM, at least 4 K blocks per CTA (a
+  // CTA's fixed cost - tensor-memory set-up, pipeline fill, hand-off - grows
+  // with the number of CTAs sharing a tile).  FQ_FORCE_SCHEDULE=dp gives every
+  // CTA one whole tile instead (no partial sums; tests and studies).
+  const int64_t by_work = (p.total + 3) / 4;
+  int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
+  if (const char* f = std::getenv("FQ_FORCE_SCHEDULE")) {
+    if (!std::strcmp(f, "dp") && tiles <= es::kMaxGrid) grid = int(tiles);
+    // each tile split in two halves (partial sums: the workspace holds two slots per SM)
+    if (!std::strcmp(f, "k2") && 2 * tiles <= d.sm_count) grid = int(2 * tiles);
+  }
+  // partial-sum slots exist for sm_count CTAs; only whole-tile CTAs (grid == tiles) may exceed that
+  if (grid > d.sm_count && grid != tiles) return FQ_ERR_SHAPE;
   const bool pdl = pdl_enabled();
   cudaError_t e;
-  if (data_parallel) {
-    switch (mt) {
-      case 8: e = es::launch_es<8, 4>(tw, tx, p, grid, s, pdl); break;
-      case 16: e = es::launch_es<16, 4>(tw, tx, p, grid, s, pdl); break;
-      case 32: e = es::launch_es<32, 4>(tw, tx, p, grid, s, pdl); break;
-      default: e = es::launch_es<64, 4>(tw, tx, p, grid, s, pdl); break;
-    }
-  } else {
-    switch (mt) {
-      case 8: e = es::launch_es<8, 8>(tw, tx, p, grid, s, pdl); break;
-      case 16: e = es::launch_es<16, 8>(tw, tx, p, grid, s, pdl); break;
-      case 32: e = es::launch_es<32, 8>(tw, tx, p, grid, s, pdl); break;
-      default: e = es::launch_es<64, 8>(tw, tx, p, grid, s, pdl); break;
-    }
+  switch (mt) {
+    case 16: e = es::launch_es<16>(&tw_map, &tx_map, p, fmt, grid, s, pdl); break;
+    case 32: e = es::launch_es<32>(&tw_map, &tx_map, p, fmt, grid, s, pdl); break;
+    default: e = es::launch_es<64>(&tw_map, &tx_map, p, fmt, grid, s, pdl); break;
   }
   return cuda_status(e);
 }

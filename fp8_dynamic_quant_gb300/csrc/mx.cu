@@ -67,14 +67,6 @@ __device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
   return lo;
 }
 
-// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
 // Scale chunk (32 rows x 16 bytes, no swizzle, 8-row groups 128 bytes apart)
 // -> tensor memory: every lane quarter receives the 32 x 128-bit block.
 __device__ __forceinline__ void sf_copy(uint32_t taddr, uint32_t saddr) {

@@ -15,6 +15,9 @@
 //
 // All are HBM-streaming kernels: 16-byte coalesced loads and stores,
 // warp-shuffle reductions, grids sized to a multiple of the SM count.
+#include <cstdlib>
+#include <cstring>
+
 #include "fq_common.cuh"
 
 namespace fq {
@@ -44,8 +47,8 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 // so a call whose output could be that weight (the public entry point: a
 // per-row quant of W is the per-channel weight quant) lets the next kernel
 // start only once it has finished.
-template <int VPT>
-__global__ void __launch_bounds__(256) dynamic_quant_int8_kernel(const uint4* __restrict__ x, int64_t M,
+template <int VPT, int MAXT = 256>
+__global__ void __launch_bounds__(MAXT) dynamic_quant_int8_kernel(const uint4* __restrict__ x, int64_t M,
                                                                   int64_t K8, uint2* __restrict__ q,
                                                                   float* __restrict__ s, int trigger) {
   __shared__ float red[32];
@@ -90,6 +93,241 @@ __global__ void __launch_bounds__(256) dynamic_quant_int8_kernel(const uint4* __
       unpack8(xr[idx], f);
       qr[idx] = quant8_i8(f, sc, inv);
     }
+  }
+}
+
+// Many rows (M above the SM count): one CTA per row as above, grid-stride,
+// with the next row's loads issued before the current row is reduced and
+// stored, so each CTA keeps two rows of loads in flight; the block reduction
+// scratch alternates between two buffers, which saves its trailing barrier.
+template <int VPT, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) quant_int8_stream_kernel(const uint4* __restrict__ x, int64_t M, int64_t K8,
+                                                                 uint2* __restrict__ q, float* __restrict__ s,
+                                                                 int trigger) {
+  __shared__ float red[2][32];
+  pdl_wait();
+  if (trigger) pdl_launch_dependents();
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
+  int64_t row = blockIdx.x;
+  if (row >= M) return;
+  uint4 cur[VPT], nxt[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int64_t idx = tid + int64_t(i) * nt;
+    cur[i] = idx < K8 ? ld_stream(x + row * K8 + idx) : make_uint4(0, 0, 0, 0);
+  }
+  for (int par = 0; row < M; row += gridDim.x, par ^= 1) {
+    const int64_t next = row + gridDim.x;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * nt;
+      nxt[i] = (next < M && idx < K8) ? ld_stream(x + next * K8 + idx) : make_uint4(0, 0, 0, 0);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      float f[8];
+      unpack8(cur[i], f);
+      amax = fmaxf(amax, absmax8(f));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (lane == 0) red[par][warp] = amax;
+    __syncthreads();
+    float r = lane < nw ? red[par][lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
+    const float sc = __fdiv_rn(r, 127.0f);
+    const float inv = __frcp_rn(sc);
+    if (tid == 0) s[row] = sc;
+    uint2* qr = q + row * K8;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * nt;
+      if (idx < K8) {
+        float f[8];
+        unpack8(cur[i], f);
+        qr[idx] = quant8_i8(f, sc, inv);
+      }
+      cur[i] = nxt[i];
+    }
+  }
+}
+
+// Many rows, rows of up to 8192 elements: each row is staged into a ring of
+// R shared-memory slots by a 1-D bulk copy (the TMA engine) that one thread
+// issues R rows ahead, so a CTA keeps R rows of loads in flight (3 CTAs of a
+// 64 KB ring per SM: ~190 KB, enough to cover loaded HBM latency) while its
+// threads reduce and quantize the oldest.  Rows of this CTA: blockIdx.x +
+// i * gridDim.x.  Every thread waits (bounded) on the slot's barrier; a
+// barrier that also votes on those waits keeps all threads in step if one
+// gives up, and the copies still in flight are then drained before exit.
+constexpr int kRingMax = 16;
+template <int VPT>
+__global__ void __launch_bounds__(256, 3) quant_int8_ring_kernel(const uint4* __restrict__ x, int64_t M, int64_t K8,
+                                                                 uint2* __restrict__ q, float* __restrict__ s,
+                                                                 int trigger, int R, uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[kRingMax];
+  __shared__ float red[2][8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  const uint32_t row_bytes = uint32_t(K8) * 16u;
+  if (tid == 0) {
+    for (int i = 0; i < R; ++i) mbar_init(&full[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (trigger) pdl_launch_dependents();
+  const int64_t G = gridDim.x;
+  const int64_t nrows = M > int64_t(blockIdx.x) ? (M - 1 - blockIdx.x) / G + 1 : 0;
+  if (tid == 0) {
+    for (int64_t i = 0; i < nrows && i < R; ++i) {
+      mbar_arrive_expect_tx(&full[i], row_bytes);
+      bulk_load(ring + i * row_bytes, x + (blockIdx.x + i * G) * K8, row_bytes, &full[i]);
+    }
+  }
+  for (int64_t i = 0; i < nrows; ++i) {
+    const int slot = int(i % R);
+    const int64_t row = blockIdx.x + i * G;
+    const bool ok = mbar_wait(&full[slot], uint32_t((i / R) & 1));
+    const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(slot) * row_bytes);
+    uint4 v[VPT];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int64_t idx = tid + 256 * j;
+      v[j] = (ok && idx < K8) ? src[idx] : make_uint4(0, 0, 0, 0);
+      float f[8];
+      unpack8(v[j], f);
+      amax = fmaxf(amax, absmax8(f));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (lane == 0) red[i & 1][warp] = amax;
+    fence_proxy_async_smem();  // this thread's reads of the slot, before its async refill
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicOr(err, DEVERR_TIMEOUT);
+        // drain the copies still in flight (bounded) before the CTA exits
+        for (int64_t j = i; j < nrows && j < i + R; ++j) mbar_wait(&full[j % R], uint32_t((j / R) & 1));
+      }
+      return;
+    }
+    if (tid == 0 && i + R < nrows) {
+      mbar_arrive_expect_tx(&full[slot], row_bytes);
+      bulk_load(ring + size_t(slot) * row_bytes, x + (row + R * G) * K8, row_bytes, &full[slot]);
+    }
+    float r = lane < nw ? red[i & 1][lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r = fmaxf(r, __shfl_xor_sync(0xFFFFFFFFu, r, o));
+    const float sc = __fdiv_rn(r, 127.0f);
+    const float inv = __frcp_rn(sc);
+    if (tid == 0) s[row] = sc;
+    uint2* qr = q + row * K8;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+      const int64_t idx = tid + 256 * j;
+      if (idx < K8) {
+        float f[8];
+        unpack8(v[j], f);
+        qr[idx] = quant8_i8(f, sc, inv);
+      }
+    }
+  }
+}
+
+// One warp per row, for rows of up to 32 * VPL 16-byte vectors (K <= 4096 at
+// VPL = 16): every load of the row is issued before its absmax is needed,
+// the absmax is a warp shuffle reduction (no block barrier), and the CTA's
+// WARPS warps keep as many rows in flight - at K = 4096, 12 rows (96 KB) per
+// SM, enough to cover loaded HBM latency.
+template <int VPL, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1) quant_int8_warp_kernel(const uint4* __restrict__ x, int64_t M, int64_t K8,
+                                                               uint2* __restrict__ q, float* __restrict__ s,
+                                                               int trigger) {
+  pdl_wait();
+  if (trigger) pdl_launch_dependents();
+  const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t row = int64_t(blockIdx.x) * warps + (threadIdx.x >> 5); row < M; row += int64_t(gridDim.x) * warps) {
+    const uint4* xr = x + row * K8;
+    uint4 v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int64_t idx = lane + 32 * i;
+      v[i] = idx < K8 ? ld_stream(xr + idx) : make_uint4(0, 0, 0, 0);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float f[8];
+      unpack8(v[i], f);
+      amax = fmaxf(amax, absmax8(f));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float sc = __fdiv_rn(amax, 127.0f);
+    const float inv = __frcp_rn(sc);
+    if (lane == 0) s[row] = sc;
+    uint2* qr = q + row * K8;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int64_t idx = lane + 32 * i;
+      if (idx < K8) {
+        float f[8];
+        unpack8(v[i], f);
+        qr[idx] = quant8_i8(f, sc, inv);
+      }
+    }
+  }
+}
+
+// Small M: each row split along K over a cluster of CS CTAs (one 16-byte
+// vector per thread), so M = 1..8 rows occupy CS * M SMs.  Each CTA reduces
+// its slice, writes its partial absmax into every cluster member's shared
+// memory (distributed shared memory), and after one cluster barrier each
+// takes the max of the CS partials - the same value in every member - and
+// quantizes its slice.  CTA rank 0 writes the scale.
+template <int CS>
+__global__ void __launch_bounds__(256) quant_int8_split_kernel(const uint4* __restrict__ x, int64_t M, int64_t K8,
+                                                                uint2* __restrict__ q, float* __restrict__ s,
+                                                                int trigger) {
+  __shared__ float part[CS];
+  __shared__ float red[8];
+  // every member has started before anyone writes into its shared memory
+  cluster_arrive_relaxed();
+  pdl_wait();
+  if (trigger) pdl_launch_dependents();
+  const uint32_t rank = cluster_ctarank();
+  const int64_t row = blockIdx.x / CS;
+  const int64_t per = (K8 + CS - 1) / CS;  // vectors per member
+  const int64_t idx = int64_t(rank) * per + threadIdx.x;
+  const bool mine = threadIdx.x < per && idx < K8 && row < M;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (mine) v = ld_stream(x + row * K8 + idx);
+  float f[8];
+  unpack8(v, f);
+  float amax = absmax8(f);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  cluster_wait_acquire();
+  if (threadIdx.x < CS) {
+    float m = 0.0f;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    st_cluster_u32(mapa_shared(smem_u32(&part[rank]), uint32_t(threadIdx.x)), __float_as_uint(m));
+  }
+  cluster_sync_all();  // partials delivered (release / acquire across the cluster)
+  float tot = 0.0f;
+#pragma unroll
+  for (int c = 0; c < CS; ++c) tot = fmaxf(tot, part[c]);
+  const float sc = __fdiv_rn(tot, 127.0f);
+  const float inv = __frcp_rn(sc);
+  if (row < M) {
+    if (rank == 0 && threadIdx.x == 0) s[row] = sc;
+    if (mine) q[row * K8 + idx] = quant8_i8(f, sc, inv);
   }
 }
 
@@ -627,6 +865,36 @@ using namespace fq;
 
 // ================================================================ entry points
 
+// Kernel choice for the per-token INT8 quant (FQ_QUANT_KERNEL = wide | row |
+// ring | warp | split overrides it; tests and studies).  Measured on GB300,
+// each call in a CUDA graph (us per call at M = 1..64, K = 4096 / K = 1024;
+// M = 16384, K = 4096):
+//  * few rows (M <= SM count): one CTA per row with up to 1024 threads, one
+//    16-byte vector a thread for K <= 8192 ("wide"): 1.96-2.15 / 1.79-2.06.
+//    A decode-sized row is one round trip to memory; what remains on the
+//    critical path is the per-thread quant arithmetic and the block barrier.
+//  * many rows: CTAs of 256 threads, grid-stride over rows, the next row's
+//    loads in flight while the current one is reduced and stored ("row"):
+//    60 us at M = 16384 (0.49 of HBM).
+//  * built, tested, taken only when forced: 256-thread rows without the
+//    prefetch (2.35-2.8 / 1.82-2.2; 66.5 us), rows staged through a
+//    shared-memory ring by bulk copies 8-16 rows ahead ("ring", 70 us), one
+//    warp per row ("warp": a lane quantizes 128 values one after the other,
+//    7.2 us at M = 1) and the row split along K over a cluster with a
+//    distributed-shared-memory absmax exchange ("split", M <= 8: 2.1-2.45 /
+//    2.15-2.4 - the cluster barriers cost what the split saves).
+enum QuantKernel { QK_AUTO = 0, QK_WIDE = 1, QK_ROW = 2, QK_WARP = 3, QK_SPLIT = 4, QK_RING = 5 };
+static int forced_quant_kernel() {
+  const char* v = std::getenv("FQ_QUANT_KERNEL");
+  if (!v) return QK_AUTO;
+  if (!std::strcmp(v, "wide")) return QK_WIDE;
+  if (!std::strcmp(v, "row")) return QK_ROW;
+  if (!std::strcmp(v, "warp")) return QK_WARP;
+  if (!std::strcmp(v, "split")) return QK_SPLIT;
+  if (!std::strcmp(v, "ring")) return QK_RING;
+  return QK_AUTO;
+}
+
 fq_status fq::quant_int8_launch(const uint16_t* x, int64_t M, int64_t K, int8_t* xq, float* sx, fq_stream_t stream,
                             bool trigger) {
   if (M < 0 || K < 0 || K % 16 || K > (int64_t(1) << 30) || M > (int64_t(1) << 40)) return FQ_ERR_SHAPE;
@@ -638,22 +906,93 @@ fq_status fq::quant_int8_launch(const uint16_t* x, int64_t M, int64_t K, int8_t*
   if (st != FQ_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t K8 = K / 8;
-  const int threads = K8 >= 256 ? 256 : (K8 >= 128 ? 128 : (K8 >= 64 ? 64 : 32));
-  const int grid = grid_for(M, 1, d.sm_count, 2048 / threads);
-  const int64_t vpt = (K8 + threads - 1) / threads;
   const bool pdl = pdl_enabled();
   cudaError_t e;
   auto xp = reinterpret_cast<const uint4*>(x);
   auto qp = reinterpret_cast<uint2*>(xq);
   const int tr = trigger ? 1 : 0;
-  if (vpt <= 1)
-    e = launch(dynamic_quant_int8_kernel<1>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
-  else if (vpt <= 2)
-    e = launch(dynamic_quant_int8_kernel<2>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
-  else if (vpt <= 4)
-    e = launch(dynamic_quant_int8_kernel<4>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
-  else
-    e = launch(dynamic_quant_int8_kernel<8>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
+  int force = forced_quant_kernel();
+  if (force == QK_SPLIT && !(M <= 8 && K8 > 0 && K8 <= 2048)) force = QK_AUTO;
+  if (force == QK_WARP && K8 > 512) force = QK_AUTO;
+  if (force == QK_RING && !(K8 > 0 && K8 <= 1024)) force = QK_AUTO;
+  if (force == QK_WIDE && K8 > 4096) force = QK_AUTO;
+  if (force == QK_ROW && K8 > 1024) force = QK_AUTO;
+  if (force == QK_AUTO) force = M <= d.sm_count ? (K8 <= 4096 ? QK_WIDE : QK_AUTO) : (K8 <= 1024 ? QK_ROW : QK_AUTO);
+  if (force == QK_SPLIT) {
+    // 8 CTAs per row when each gets at least 64 vectors, else 4 or 2
+    const int cs = K8 >= 512 ? 8 : (K8 >= 256 ? 4 : 2);
+    const int64_t per = (K8 + cs - 1) / cs;
+    const int threads = per > 128 ? 256 : (per > 64 ? 128 : (per > 32 ? 64 : 32));
+    const int grid = int(M) * cs;
+    e = cs == 8 ? launch_cluster(quant_int8_split_kernel<8>, grid, threads, 0, s, pdl, 8u, xp, M, K8, qp, sx, tr)
+        : cs == 4 ? launch_cluster(quant_int8_split_kernel<4>, grid, threads, 0, s, pdl, 4u, xp, M, K8, qp, sx, tr)
+                  : launch_cluster(quant_int8_split_kernel<2>, grid, threads, 0, s, pdl, 2u, xp, M, K8, qp, sx, tr);
+    return cuda_status(e);
+  }
+  if (force == QK_WARP) {
+    const int vpl = int((K8 + 31) / 32);
+    const int warps = vpl > 8 ? 12 : 16;  // registers: 16 vectors a lane hold 64 of them
+    const int64_t ctas = (M + warps - 1) / warps;
+    const int grid = int(ctas < int64_t(d.sm_count) * 2 ? ctas : int64_t(d.sm_count) * 2);
+    if (vpl <= 1)
+      e = launch(quant_int8_warp_kernel<1, 16>, grid, 32 * warps, 0, s, pdl, xp, M, K8, qp, sx, tr);
+    else if (vpl <= 2)
+      e = launch(quant_int8_warp_kernel<2, 16>, grid, 32 * warps, 0, s, pdl, xp, M, K8, qp, sx, tr);
+    else if (vpl <= 4)
+      e = launch(quant_int8_warp_kernel<4, 16>, grid, 32 * warps, 0, s, pdl, xp, M, K8, qp, sx, tr);
+    else if (vpl <= 8)
+      e = launch(quant_int8_warp_kernel<8, 16>, grid, 32 * warps, 0, s, pdl, xp, M, K8, qp, sx, tr);
+    else
+      e = launch(quant_int8_warp_kernel<16, 12>, grid, 32 * warps, 0, s, pdl, xp, M, K8, qp, sx, tr);
+    return cuda_status(e);
+  }
+  if (force == QK_RING) {
+    const size_t row_bytes = size_t(K8) * 16;
+    int R = int(65536 / row_bytes);
+    R = R < 2 ? 2 : (R > kRingMax ? kRingMax : R);
+    const size_t smem = size_t(R) * row_bytes;
+    const int grid = grid_for(M, 1, d.sm_count, 3);
+    const int vpt = int((K8 + 255) / 256);
+    auto k = vpt <= 1 ? quant_int8_ring_kernel<1> : (vpt <= 2 ? quant_int8_ring_kernel<2> : quant_int8_ring_kernel<4>);
+    static uint64_t attr_done[3] = {0, 0, 0};
+    const int ki = vpt <= 1 ? 0 : (vpt <= 2 ? 1 : 2);
+    if (!(attr_done[ki] & (1ull << (d.id & 63)))) {
+      if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536)) != cudaSuccess)
+        return cuda_status(e);
+      attr_done[ki] |= 1ull << (d.id & 63);
+    }
+    e = launch(k, grid, 256, smem, s, pdl, xp, M, K8, qp, sx, tr, R, d.err_word);
+    return cuda_status(e);
+  }
+  if (force == QK_WIDE || force == QK_ROW) {
+    // WIDE: up to 1024 threads, one vector each while K <= 8192; ROW: 256 threads
+    const int64_t t32 = (K8 + 31) / 32 * 32;
+    const int threads = force == QK_ROW ? (K8 >= 256 ? 256 : int(t32)) : int(t32 < 1024 ? t32 : 1024);
+    const int64_t vpt = (K8 + threads - 1) / threads;
+    if (force == QK_ROW) {
+      const int grid = grid_for(M, 1, d.sm_count, 6 * 256 / threads);
+      if (vpt <= 1)
+        e = launch(quant_int8_stream_kernel<1, 256, 6>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
+      else if (vpt <= 2)
+        e = launch(quant_int8_stream_kernel<2, 256, 6>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
+      else
+        e = launch(quant_int8_stream_kernel<4, 256, 6>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
+    } else {
+      const int grid = grid_for(M, 1, d.sm_count, 2048 / threads);
+      if (vpt <= 1)
+        e = launch(quant_int8_stream_kernel<1, 1024, 1>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
+      else if (vpt <= 2)
+        e = launch(quant_int8_stream_kernel<2, 1024, 1>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
+      else
+        e = launch(quant_int8_stream_kernel<4, 1024, 1>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
+    }
+    return cuda_status(e);
+  }
+  // long rows (K > 8192 with many rows, K > 32768 with few): one CTA per row
+  // re-reading the part of the row its registers do not hold
+  const int threads = 256;
+  const int grid = grid_for(M, 1, d.sm_count, 2048 / threads);
+  e = launch(dynamic_quant_int8_kernel<8>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);
   return cuda_status(e);
 }
 

@@ -34,6 +34,32 @@ def test_dynamic_quant_bit_exact(M, K):
     assert np.array_equal(q, oq)
 
 
+@pytest.mark.parametrize("kernel", ["wide", "row", "ring", "warp", "split"])
+@pytest.mark.parametrize("M,K", [(1, 4096), (2, 1024), (3, 4096), (4, 4096), (7, 1024), (8, 4096), (1, 16),
+                                 (5, 48), (8, 16384), (6, 2064), (64, 4096), (1300, 1024), (33, 4112),
+                                 (2000, 8192), (1217, 16), (999, 2064)])
+def test_dynamic_quant_every_kernel(kernel, M, K, monkeypatch):
+    """Each quant kernel forced on the same rows (a kernel the shape cannot take
+    falls back to the automatic choice): one CTA of up to 1024 threads per row,
+    256-thread rows with the next row prefetched, rows staged through a
+    shared-memory ring by bulk copies, one warp per row, and the row split along
+    K over a cluster (M <= 8)."""
+    monkeypatch.setenv("FQ_QUANT_KERNEL", kernel)
+    x = synth.activations(M, K, 1500 + M * 5 + K)
+    q, s = gpu_quant(x)
+    oq, os_ = oi8.dynamic_quant_int8(x)
+    assert np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(q, oq)
+    # the fused op's two-launch path runs the same quant kernel
+    if K % 16 == 0 and K <= 4096:
+        w = synth.uniform_int8((32, K), 7)
+        sw = synth.channel_scales(32, 8)
+        y, xq, sx = fq.w8a8_quant_linear(bf16_to_dev(x), np_to_dev(w), np_to_dev(sw), return_quant=True)
+        assert np.array_equal(xq.cpu().numpy(), oq) and np.array_equal(sx.cpu().numpy().view(np.uint32),
+                                                                       os_.view(np.uint32))
+        assert np.array_equal(bf16_to_np(y), oi8.w8a8_linear(oq, os_, w, sw))
+
+
 def test_dynamic_quant_edge_rows():
     import json, os
     d = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "int8_rows.json")))
