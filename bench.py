@@ -97,6 +97,55 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+ENGINES = [(0, "mma_sync_f16_m16n8k16"), (1, "mma_sync_e4m3_m16n8k32"), (2, "mma_sync_s8_m16n8k32"),
+           (3, "tcgen05_f16_128x256x16"), (4, "tcgen05_f8f6f4_128x256x32"), (5, "tcgen05_f16_128x64x16"),
+           (6, "tcgen05_f8f6f4_128x16x32")]
+
+
+def engine_peaks(torch, dev):
+    """Measured throughput (TFLOP/s, TOPS for s8) of each matrix engine the kernels use, from
+    libfq_peaks.so: mma.sync with 8 warps x 4 CTAs per SM and 8 independent chains a warp; tcgen05 with
+    one issuing thread per SM.  Each kernel is sized to run ~1 ms and timed with CUDA events."""
+    import ctypes
+    from fp8_dynamic_quant_gb300 import build as fqbuild
+    if not os.path.exists(fqbuild.PEAKS_LIB):
+        return None
+    L = ctypes.CDLL(fqbuild.PEAKS_LIB)
+    L.fq_peak_run.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                              ctypes.POINTER(ctypes.c_double), ctypes.c_void_p, ctypes.c_void_p]
+    L.fq_peak_run.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sink = torch.zeros(256, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for kind, name in ENGINES:
+        ctas = sms * 4 if kind <= 2 else sms
+        ops = ctypes.c_double(0)
+
+        def run(iters):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            rc = L.fq_peak_run(kind, iters, ctas, ctypes.c_void_p(stream.cuda_stream), ctypes.byref(ops),
+                               ctypes.c_void_p(err.data_ptr()), ctypes.c_void_p(sink.data_ptr()))
+            b.record()
+            torch.cuda.synchronize()
+            if rc != 0:
+                raise RuntimeError("fq_peak_run(%d) failed: %d" % (kind, rc))
+            return a.elapsed_time(b)
+        iters = 64
+        run(iters)
+        ms = run(iters)
+        iters = max(64, int(iters * 1.0 / max(ms, 1e-3)))       # about 1 ms
+        run(iters)
+        ms = min(run(iters) for _ in range(3))
+        out[name] = round(ops.value / (ms * 1e-3) / 1e12, 1)
+    if int(err.item()) != 0:
+        return None
+    out["unit"] = "TFLOP/s (s8: TOPS), measured on this GPU"
+    return out
+
+
 def traffic_for(kernel_key, sources):
     """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -109,6 +158,32 @@ def traffic_for(kernel_key, sources):
     for s in sources:
         h.update(open(os.path.join(ROOT, s), "rb").read())
     return d["dram_bytes_per_launch"] if d.get("source_sha256") == h.hexdigest() else None
+
+
+def library_schedules(fn, torch):
+    """Runs fn() once with FQ_DEBUG_SCHEDULE=1 and returns the schedule the
+    library reported for each W8A8 call, in call order (read from its stderr)."""
+    import tempfile
+    sys.stderr.flush()
+    saved = os.dup(2)
+    old = os.environ.get("FQ_DEBUG_SCHEDULE")
+    with tempfile.TemporaryFile(mode="w+") as tmp:
+        os.dup2(tmp.fileno(), 2)
+        os.environ["FQ_DEBUG_SCHEDULE"] = "1"
+        try:
+            fn()
+            torch.cuda.synchronize()
+        finally:
+            sys.stderr.flush()
+            os.dup2(saved, 2)
+            os.close(saved)
+            if old is None:
+                del os.environ["FQ_DEBUG_SCHEDULE"]
+            else:
+                os.environ["FQ_DEBUG_SCHEDULE"] = old
+        tmp.seek(0)
+        lines = [l for l in tmp.read().splitlines() if l.startswith("fq: ")]
+    return [l.split("schedule=")[1].split()[0] for l in lines]
 
 
 # ---------------------------------------------------------------- clocks
@@ -218,14 +293,16 @@ def run_fq(args, rank, world, local_rank):
     def call_fused(K, N, M, c):
         fq.w8a8_quant_linear(X[(K, N, M)], W[(K, N)][c], SW[(K, N)][c], y=YF[(K, N, M)], ws=ws)
 
-    # launches per fused call: the library runs the fused op as one launch when
-    # the dense schedule streams one whole 224-row tile per CTA with 8-token
-    # tiles (M <= 8, K <= 1024, 3/4 to 1 tile per SM), else quant + GEMM
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # launches per fused call, as the library reports its own schedule choice
+    # (FQ_DEBUG_SCHEDULE): "dp224+quant" is one launch, anything else a quant
+    # launch plus a GEMM launch
+    fused_sched = library_schedules(lambda: [call_fused(K, N, M, 10 + i) for (K, N) in LINEARS
+                                             for i, M in enumerate(MS)], torch)
+    fused_n = {key: (1 if "dp224+quant" in sched else 2) for key, sched in
+               zip([(K, N, M) for (K, N) in LINEARS for M in MS], fused_sched)}
 
     def fused_launches(M, K, N):
-        tiles = (N + 223) // 224
-        return 1 if (M <= 8 and K <= 1024 and tiles <= sms and 4 * tiles >= 3 * sms) else 2
+        return fused_n[(K, N, M)]
 
     small, big = LINEARS
     groups = [
@@ -307,7 +384,18 @@ def run_fq(args, rank, world, local_rank):
     dom_ms = group_ms[2]
     dom_bytes_per_launch = groups[2][2] / len(MS)
     achieved = dom_bytes_per_launch / (dom_ms * 1e-3 / len(MS)) / 1e9
-    roofline = {"kernel": "w8a8_gemm_kernel (K=1024, N=32768, M in 1..64)", "bound": "hbm",
+    big_sched = library_schedules(lambda: [call_gemm(*big, M, i) for i, M in enumerate(MS)], torch)
+    kern = {"dp224": "w8a8_gemm_kernel<MT,14> (224-row tiles)", "umma": "w8a8_umma_kernel (tcgen05)",
+            "streamk": "w8a8_gemm_kernel<MT,8> (stream-K)", "cluster4": "w8a8_cluster_kernel"}
+    ran = []
+    for sch, M in zip(big_sched, MS):
+        name = kern.get(sch, sch)
+        if not ran or ran[-1][0] != name:
+            ran.append([name, []])
+        ran[-1][1].append(M)
+    roofline = {"kernel": "W8A8 GEMM on (K=1024, N=32768), M in 1..64: " +
+                          "; ".join("%s at M=%s" % (n, ",".join(map(str, ms))) for n, ms in ran),
+                "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": hbm_peak, "peak_source": peak_src + " hbm_gbs",
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 3),
                 "traffic": traffic_for("w8a8_gemm_kernel@K1024xN32768",
@@ -319,20 +407,24 @@ def run_fq(args, rank, world, local_rank):
     out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K_steps,
            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-           "config": {"workload": "INT8 W8A8 M-sweep: per-token quant, W8A8 GEMM and fused quant+GEMM on "
-                                  "(K=4096,N=1024) and (K=1024,N=32768), M in {1,2,3,4,7,8,9,16,32,64}",
-                      "linears": [list(l) for l in LINEARS], "M": MS,
-                      "bytes_per_step": sb,
-                      "l2": "each call reads its own weight copy; %d MB of weights per step (> 2x the %d MB L2) "
-                            "so every call streams weights from HBM; activations L2-hot" %
-                            (sum(K * N for (K, N) in LINEARS) * 20 // 2 ** 20, l2 // 2 ** 20),
-                      "timing": "op groups captured as CUDA graphs, replayed; CUDA events",
-                      "parallelism": "replicas" if world > 1 else "single GPU"},
+           "config": workload_config(),
+           "timing": "op groups captured as CUDA graphs, replayed; CUDA events on the launching stream",
+           "parallelism": "replicas" if world > 1 else "single GPU",
            "gpu_launches": launches_per_step * K_steps,
            "groups": group_report, "roofline": roofline}
     clk = clocks.summary(w0, w1)
     out["clocks"] = clk
 
+    if rank == 0:
+        out["engine_peaks"] = engine_peaks(torch, dev)
+        ep = out["engine_peaks"] or {}
+        # compute term of the roofline kernel: 2MNK per launch against the engine it runs on
+        ops = sum(2.0 * M * big[0] * big[1] for M in MS) / len(MS)
+        eng = ep.get("mma_sync_f16_m16n8k16")
+        roofline["compute"] = {"ops_per_launch": ops, "engine": "mma.sync f16 (M<=32) / tcgen05 kind::f16 (M=64)",
+                               "engine_peak_tflops": eng,
+                               "achieved_tflops": round(ops / (dom_ms * 1e-3 / len(MS)) / 1e12, 2),
+                               "frac": round(ops / (dom_ms * 1e-3 / len(MS)) / 1e12 / eng, 4) if eng else None}
     if rank == 0 and not args.no_extras:
         out["per_call"] = per_call_breakdown(fq, torch, dev, W, SW, X, XQ, SX, Y, YF, ws, hbm_peak)
         out["other_configs"] = other_configs(fq, synth, torch, dev, bf, l2, hbm_peak)
@@ -365,14 +457,32 @@ def time_graph(torch, fn, reps=3, calls=1):
     return statistics.median(ts)
 
 
+def time_eager(torch, fn, calls, reps=3):
+    """Microseconds per call of `calls` eager calls issued back to back (fn issues them), CUDA events
+    on the current stream, median of reps: the launch floor the graph series hides."""
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3 / calls)
+    return statistics.median(ts)
+
+
 def per_call_breakdown(fq, torch, dev, W, SW, X, XQ, SX, Y, YF, ws, hbm_peak):
-    """Microseconds and GB/s per call for every (op, linear, M), each call on a different weight copy."""
+    """Microseconds and GB/s per call for every (op, linear, M), each call on a different weight copy:
+    CUDA-graph replays (the *_us series) and the same calls issued eagerly (*_eager_us)."""
     res = {}
     for (K, N) in LINEARS:
         nc = len(W[(K, N)])
         key = "K%d_N%d" % (K, N)
         res[key] = {"M": MS, "quant_us": [], "gemm_us": [], "fused_us": [], "gemm_GBps": [], "fused_GBps": [],
-                    "gemm_frac_hbm": [], "fused_frac_hbm": [], "weight_copies_per_graph": nc}
+                    "gemm_frac_hbm": [], "fused_frac_hbm": [], "quant_eager_us": [], "gemm_eager_us": [],
+                    "fused_eager_us": [], "weight_copies_per_graph": nc}
         for M in MS:
             R = 16
             tq = time_graph(torch, lambda: [fq.dynamic_quant_int8(X[(K, N, M)], XQ[(K, N, M)], SX[(K, N, M)])
@@ -381,6 +491,15 @@ def per_call_breakdown(fq, torch, dev, W, SW, X, XQ, SX, Y, YF, ws, hbm_peak):
                                                            y=Y[(K, N, M)], ws=ws) for c in range(nc)], calls=nc)
             tf = time_graph(torch, lambda: [fq.w8a8_quant_linear(X[(K, N, M)], W[(K, N)][c], SW[(K, N)][c],
                                                                  y=YF[(K, N, M)], ws=ws) for c in range(nc)], calls=nc)
+            eq = time_eager(torch, lambda: [fq.dynamic_quant_int8(X[(K, N, M)], XQ[(K, N, M)], SX[(K, N, M)])
+                                            for _ in range(R)], R)
+            eg = time_eager(torch, lambda: [fq.w8a8_linear(XQ[(K, N, M)], SX[(K, N, M)], W[(K, N)][c], SW[(K, N)][c],
+                                                           y=Y[(K, N, M)], ws=ws) for c in range(nc)], nc)
+            ef = time_eager(torch, lambda: [fq.w8a8_quant_linear(X[(K, N, M)], W[(K, N)][c], SW[(K, N)][c],
+                                                                 y=YF[(K, N, M)], ws=ws) for c in range(nc)], nc)
+            res[key]["quant_eager_us"].append(round(eq, 2))
+            res[key]["gemm_eager_us"].append(round(eg, 2))
+            res[key]["fused_eager_us"].append(round(ef, 2))
             gb = bytes_gemm(M, K, N) / (tg * 1e-6) / 1e9
             fb = bytes_fused(M, K, N) / (tf * 1e-6) / 1e9
             res[key]["quant_us"].append(round(tq, 2))
@@ -602,7 +721,7 @@ def e2e(fq, torch, dev, W, SW, X, ws, args):
 
     for _ in range(3):
         one_step()
-    n = max(3, min(50, args.steps // 20))
+    n = max(20, min(200, args.steps // 20))
     t0 = time.perf_counter()
     for _ in range(n):
         one_step()
@@ -613,17 +732,33 @@ def e2e(fq, torch, dev, W, SW, X, ws, args):
 
 
 # ---------------------------------------------------------------- the oracle (CPU baseline / reference arm)
-def oracle_calls():
-    """The headline step as a list of oracle calls: (label, fn, algorithmic bytes)."""
+BLAS_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                    "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")
+
+
+def oracle_workload(path):
+    """Writes the headline step's oracle inputs (numpy arrays) to `path` (.npz)."""
     import numpy as np
     from fp8_dynamic_quant_gb300 import synth
+    arrs = {}
+    for (K, N) in LINEARS:
+        arrs["w_%d_%d" % (K, N)] = synth.uniform_int8((N, K), SEED + K + N)
+        arrs["sw_%d_%d" % (K, N)] = synth.channel_scales(N, SEED + 7 + N)
+        for M in MS:
+            arrs["x_%d_%d" % (K, M)] = synth.activations(M, K, SEED + 1000 + M + K)
+    np.savez(path, **arrs)
+
+
+def oracle_calls(path):
+    """The headline step as a list of oracle calls (label, fn, algorithmic bytes), inputs read from `path`."""
+    import numpy as np
     from oracle import int8 as oi8
+    a = np.load(path)
     calls = []
     for (K, N) in LINEARS:
-        w = synth.uniform_int8((N, K), SEED + K + N)
-        sw = synth.channel_scales(N, SEED + 7 + N)
+        w, sw = a["w_%d_%d" % (K, N)], a["sw_%d_%d" % (K, N)]
         for M in MS:
-            x = synth.activations(M, K, SEED + 1000 + M + K)
+            x = a["x_%d_%d" % (K, M)]
             q, s = oi8.dynamic_quant_int8(x)
             calls.append(("quant", (lambda x=x: oi8.dynamic_quant_int8(x)), bytes_quant(M, K)))
             calls.append(("gemm", (lambda q=q, s=s, w=w, sw=sw: oi8.w8a8_linear(q, s, w, sw)), bytes_gemm(M, K, N)))
@@ -631,59 +766,106 @@ def oracle_calls():
     return calls
 
 
-def cpu_baseline(budget_s=20.0):
-    """The oracle as it stands, on the host cores, over a bounded sample of the headline step."""
-    calls = oracle_calls()
-    done_bytes, n, t0 = 0, 0, time.perf_counter()
-    i = 0
-    while True:
-        _, fn, b = calls[i % len(calls)]
-        fn()
-        done_bytes += b
-        n += 1
-        i += 1
-        if time.perf_counter() - t0 >= budget_s and n >= len(calls):
-            break
-    dt = time.perf_counter() - t0
-    return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "%d oracle calls cycling over the %d calls of one headline step (quant, GEMM, fused per "
-                      "linear and M), %.1f s of CPU time, numpy with the host BLAS threads" % (n, len(calls), dt)}
-
-
-def run_reference(args):
-    """Reference arm: the CPU oracle, each step a bounded sample of the headline workload."""
-    calls = oracle_calls()
-    budget_total = float(os.environ.get("FQ_REF_BUDGET_S", "120"))
-    per_step = max(0.002, budget_total / max(1, args.steps + args.warmup))
-    i = 0
-
-    def one_step():
-        nonlocal i
+def _oracle_proc(path, start, rounds, seconds, barrier, results):
+    """One single-threaded oracle process: `rounds` rounds, each starting at the shared barrier and
+    running oracle calls round-robin (from call `start`) for at least `seconds`."""
+    calls = oracle_calls(path)
+    i = start
+    out = []
+    for _ in range(rounds):
+        barrier.wait()
         t0 = time.perf_counter()
-        b = 0
+        b = n = 0
         while True:
             _, fn, nb = calls[i % len(calls)]
             fn()
             b += nb
+            n += 1
             i += 1
-            if time.perf_counter() - t0 >= per_step:
-                return b
+            if time.perf_counter() - t0 >= seconds:
+                break
+        out.append((b, n, time.perf_counter() - t0))
+    results.put(out)
 
-    for _ in range(args.warmup):
-        one_step()
-    tot_b, t0 = 0, time.perf_counter()
-    for _ in range(args.steps):
-        tot_b += one_step()
-    dt = time.perf_counter() - t0
+
+def oracle_rate(workers, rounds, seconds):
+    """Runs the oracle in `workers` spawned processes, each with one BLAS thread, for `rounds` rounds
+    of about `seconds` each.  Returns per-round (bytes, calls, wall seconds) summed over the workers;
+    a round's wall time is its slowest worker's."""
+    import multiprocessing
+    import tempfile
+    ctx = multiprocessing.get_context("spawn")      # no fork after CUDA is up
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "oracle_inputs.npz")
+        oracle_workload(path)
+        saved = {v: os.environ.get(v) for v in BLAS_THREAD_VARS}
+        for v in BLAS_THREAD_VARS:
+            os.environ[v] = "1"
+        try:
+            barrier = ctx.Barrier(workers)
+            results = ctx.Queue()
+            ncalls = 3 * len(LINEARS) * len(MS)
+            procs = [ctx.Process(target=_oracle_proc, args=(path, (k * 7) % ncalls, rounds, seconds, barrier,
+                                                            results)) for k in range(workers)]
+            for p in procs:
+                p.start()
+            per = [results.get() for _ in procs]
+            for p in procs:
+                p.join()
+        finally:
+            for v, val in saved.items():
+                if val is None:
+                    os.environ.pop(v, None)
+                else:
+                    os.environ[v] = val
+    return [(sum(w[r][0] for w in per), sum(w[r][1] for w in per), max(w[r][2] for w in per))
+            for r in range(rounds)]
+
+
+def cpu_baseline(budget_s=20.0):
+    """The oracle as it stands on the host cores, over a bounded sample of the headline step: once
+    single-threaded, once in one single-threaded process per core.  The headline object is the
+    all-cores run; the single-thread run is reported beside it."""
+    ncpu = os.cpu_count() or 1
+    (b1, n1, t1), = oracle_rate(1, 1, 0.4 * budget_s)
+    (bn, nn, tn), = oracle_rate(ncpu, 1, 0.6 * budget_s)
+    return {"value": round(bn / tn / 1e9, 4), "unit": UNIT, "cores": ncpu, "kind": "oracle",
+            "sample": "%d oracle calls cycling over the 60 calls of one headline step (quant, GEMM, fused per "
+                      "linear and M) in %d single-threaded processes (one per core), %.1f s wall" % (nn, ncpu, tn),
+            "single_thread": {"value": round(b1 / t1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                              "sample": "%d oracle calls in one process with one BLAS thread, %.1f s" % (n1, t1)}}
+
+
+def workload_config():
+    """The `config` object of the bench line, the same for both arms."""
+    return {"workload": "INT8 W8A8 M-sweep: per-token quant, W8A8 GEMM and fused quant+GEMM on "
+                        "(K=4096,N=1024) and (K=1024,N=32768), M in {1,2,3,4,7,8,9,16,32,64}",
+            "linears": [list(l) for l in LINEARS], "M": MS,
+            "bytes_per_step": step_bytes(),
+            "l2": "each call reads its own weight copy; %d MB of weights per step (> 2x the 126 MB L2) so every "
+                  "call streams weights from HBM; activations L2-hot" %
+                  (sum(K * N for (K, N) in LINEARS) * 20 // 2 ** 20)}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle in one single-threaded process per host core, each step a bounded
+    round of the headline workload's oracle calls."""
+    ncpu = os.cpu_count() or 1
+    budget_total = float(os.environ.get("FQ_REF_BUDGET_S", "120"))
+    per_step = max(0.05, budget_total / max(1, args.steps + args.warmup))
+    rounds = oracle_rate(ncpu, args.warmup + args.steps, per_step)[args.warmup:]
+    tot_b = sum(r[0] for r in rounds)
+    dt = sum(r[2] for r in rounds)
+    calls = sum(r[1] for r in rounds)
     v = tot_b / dt / 1e9
-    sample = "each step runs oracle calls of the headline sweep round-robin for >= %.3f s; %d calls in all" % (per_step, i)
+    sample = ("each step: oracle calls of the headline sweep round-robin for >= %.3f s in %d single-threaded "
+              "processes (one per core); %d timed calls" % (per_step, ncpu, calls))
     return {"metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic", "impl": "reference",
-            "config": {"workload": "INT8 W8A8 M-sweep: per-token quant, W8A8 GEMM and fused quant+GEMM on "
-                                   "(K=4096,N=1024) and (K=1024,N=32768), M in {1,2,3,4,7,8,9,16,32,64}",
-                       "linears": [list(l) for l in LINEARS], "M": MS},
-            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "config": workload_config(),
+            "timing": "host wall clock per round; rounds start together at a process barrier",
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": ncpu, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

@@ -14,6 +14,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfq.so")
+# engine-peak microbenchmarks for bench.py's roofline (not part of the fq ABI)
+PEAKS_SRC = os.path.join(HERE, "peaks", "engine_peaks.cu")
+PEAKS_LIB = os.path.join(HERE, "libfq_peaks.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
@@ -39,6 +42,23 @@ def _compile(src, verbose):
     if r.returncode != 0:
         raise RuntimeError("nvcc failed on %s:\n%s%s" % (src, r.stdout, r.stderr))
     return obj, r.stderr
+
+
+def build_peaks(force=False):
+    """Compile libfq_peaks.so (bench.py's engine microbenchmarks); returns its path."""
+    deps = [PEAKS_SRC, os.path.join(CSRC, "fq_common.cuh"), __file__]
+    if not force and os.path.exists(PEAKS_LIB):
+        t = os.path.getmtime(PEAKS_LIB)
+        if all(os.path.getmtime(d) < t for d in deps if os.path.exists(d)):
+            return PEAKS_LIB
+    tmp = PEAKS_LIB + ".tmp"
+    cmd = [nvcc()] + ARCH + FLAGS + ["-shared", "-cudart", "shared", "-o", tmp, PEAKS_SRC,
+                                     "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed on %s:\n%s%s" % (PEAKS_SRC, r.stdout, r.stderr))
+    os.replace(tmp, PEAKS_LIB)
+    return PEAKS_LIB
 
 
 def build(verbose=False, force=False):
