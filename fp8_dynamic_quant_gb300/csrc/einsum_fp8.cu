@@ -98,6 +98,7 @@ struct Cfg {
 
 struct Problem {
   int T, G, D, N, KB, NB, TT, P, Ta;
+  int ahead;  // stages kept in flight (<= the ring)
   int64_t total;
   const void* sx;
   const float* sw;
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmX);
     // weights do not depend on the previous kernel: the first stages go out now
     const int b0 = int(int64_t(b) * p.total / G), b1 = int(int64_t(b + 1) * p.total / G);
-    npre = min(b1 - b0, S);
+    npre = min(b1 - b0, p.ahead);
     const uint64_t pol_w = p.TT > 1 ? policy_evict_normal() : policy_evict_first();
     int tile = b0 / p.KB, kb = b0 - tile * p.KB;
     ETile t = etile(p, tile);
@@ -246,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = r % S;
         uint8_t* st = smem + s * C::STAGE;
         if (r >= npre) {
-          // stage s held iteration r - S: wait until that iteration's group completed
+          // iteration r - ahead's group completed: at most `ahead` stages in
+          // flight, and (r - S <= r - ahead) slot s is free
           const int gl = lag.g;
           lag.advance(KB, n_it);
           if (s_abort || !mbar_wait(&grp[gl % kGroupBars], uint32_t((gl / kGroupBars) & 1))) {
@@ -596,6 +598,14 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   // CTA's fixed cost - tensor-memory set-up, pipeline fill, hand-off - grows
   // with the number of CTAs sharing a tile).  FQ_FORCE_SCHEDULE=dp gives every
   // CTA one whole tile instead (no partial sums; tests and studies).
+  // stages in flight: about 120 KB per SM (see the W8A8 GEMM's stage cap)
+  {
+    const int stage = 128 * 128 + mt * 128, ring = mt == 16 ? es::Cfg<16>::STAGES
+                                                 : (mt == 32 ? es::Cfg<32>::STAGES : es::Cfg<64>::STAGES);
+    int ah = (122880 + stage / 2) / stage;
+    if (const char* v = std::getenv("FQ_STAGES_AHEAD")) ah = std::atoi(v);
+    p.ahead = ah < 2 ? 2 : (ah > ring ? ring : ah);
+  }
   const int64_t by_work = (p.total + 3) / 4;
   int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
   if (const char* f = std::getenv("FQ_FORCE_SCHEDULE")) {

@@ -110,6 +110,7 @@ struct Problem {
   const int32_t* offsets;   // grouped: [E + 1]
   int E;                    // grouped: experts
   int w_reuse;              // weight tiles are read by more than one token tile
+  int ahead;                // stages the producer keeps in flight (0: the whole ring)
   const uint16_t* x16;      // CTA-quantized activations: bf16 [M, K]
   int8_t* xq_out;           // ... optional copy of the quantized activations [M, K]
   float* sx_out;            // ... optional copy of their scales [M]
@@ -119,6 +120,21 @@ struct Problem {
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// The same load as an ordinary (non-volatile) asm, so the compiler may issue it
+// ahead of the MMAs that precede it.  Its address must come from pin() after
+// the mbarrier wait that guards the data: the dependency keeps the load from
+// moving above the wait; a consuming volatile MMA keeps it from sinking below
+// the stage's release.
+__device__ __forceinline__ uint4 lds128_nv(uint32_t addr) {
+  uint4 v;
+  asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t pin(uint32_t v) {
+  asm volatile("" : "+r"(v)::"memory");
   return v;
 }
 
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
     if (!GROUPED) {
       // this CTA's stream-K range, as rb[] below tabulates it
       const int b0 = int(int64_t(b) * p.total / G), b1 = int(int64_t(b + 1) * p.total / G);
-      pre = min(b1 - b0, S);
+      pre = min(b1 - b0, p.ahead > 0 && p.ahead < S ? p.ahead : S);
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       int tile = b0 / p.KB, kb = b0 - tile * p.KB;
       TileCoord tc = decode_tile<MT, BN, GROUPED>(p, tile, nullptr);
@@ -318,7 +334,10 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const int n_it = end - begin;
-      const int npre = n_it < S ? n_it : S;
+      // stages kept in flight: the whole ring, or fewer so that the first
+      // ones land sooner and the consumers start while the rest stream
+      const int AH = p.ahead > 0 && p.ahead < S ? p.ahead : S;
+      const int npre = n_it < AH ? n_it : AH;
       // weights do not depend on the previous kernel: issue them first
       // (dense problems issued them at kernel entry)
       if (GROUPED) {
@@ -342,7 +361,10 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
         if (r < npre) {
           if (!FQ) tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
         } else {
-          if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
+          // iteration r - AH consumed: at most AH stages in flight, and (as
+          // r - S <= r - AH) slot s is free
+          const int rq = r - AH;
+          if (s_abort || !mbar_wait(&empty[rq % S], uint32_t((rq / S) & 1))) {
             if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
             s_abort = 1;
             break;
@@ -513,13 +535,13 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
       }
-      const uint32_t st = sbase + uint32_t(s * C::STAGE);
-      const uint32_t xo = xbase + uint32_t(s * C::XF) + uint32_t(lane * 16);
+      const uint32_t st = pin(sbase + uint32_t(s * C::STAGE));
+      const uint32_t xo = pin(xbase + uint32_t(s * C::XF) + uint32_t(lane * 16));
 #pragma unroll
       for (int h = 0; h < 2 && ok; ++h) {
         const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
-        const uint4 wa = lds128(st + rowW0 + q);
-        const uint4 wb = lds128(st + rowW1 + q);
+        const uint4 wa = lds128_nv(st + rowW0 + q);
+        const uint4 wb = lds128_nv(st + rowW1 + q);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           // B fragments of k16 steps 2*half and 2*half+1; 8-token groups past
@@ -528,7 +550,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
           uint4 xv[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j)
-            if (8 * j < rows_cur) xv[j] = lds128(xo + uint32_t(((h * NT + j) * 2 + half) * 512));
+            if (8 * j < rows_cur) xv[j] = lds128_nv(xo + uint32_t(((h * NT + j) * 2 + half) * 512));
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             const int ks = 2 * half + kk;
@@ -1526,6 +1548,18 @@ static int forced_schedule() {
   if (!std::strcmp(v, "umma")) return SCHED_UMMA;
   return SCHED_AUTO;
 }
+// Stages the producer keeps in flight.  Every CTA asking for its whole ring
+// at once (~200 KB per SM) makes HBM interleave all of them, so the first
+// stage lands only when most of the data has (~3.6 us) and the consumers
+// start late; with ~120 KB per SM in flight the bandwidth holds and the first
+// stages land sooner.  Measured on the 224-row tiles (K=1024, N=32768):
+// 4 stages 8.3-8.7 us at M <= 8 against 9.3-9.8 for the whole ring (7), 3
+// stages 8.4-9.0, 2 stages 9.6-9.8.  FQ_STAGES_AHEAD overrides (studies).
+static int stages_ahead(int stage_bytes) {
+  if (const char* v = std::getenv("FQ_STAGES_AHEAD")) return std::atoi(v);
+  const int n = (122880 + stage_bytes / 2) / stage_bytes;
+  return n < 2 ? 2 : n;
+}
 static void debug_schedule(const char* op, int64_t M, int64_t K, int64_t N, int mt, const char* sched, int grid) {
   const char* v = std::getenv("FQ_DEBUG_SCHEDULE");
   if (v && v[0] == '1')
@@ -1635,6 +1669,7 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   p.slots = static_cast<int32_t*>(slots);
   p.err = d.err_word;
   p.w_reuse = m_tiles_run > 1 ? 1 : 0;
+  p.ahead = stages_ahead(int((data_parallel ? 224 : kBN) * kBK + mt_run * kBK));
   const uint32_t bn = data_parallel ? 224u : uint32_t(kBN);
   CUtensorMap tw_map, tx_map;
   if (!tensor_map_u8_2d(&tw_map, w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, bn) ||
@@ -1744,6 +1779,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
     p.x16 = x;
     p.xq_out = xq_out;
     p.sx_out = sx_out;
+    p.ahead = stages_ahead(224 * kBK);
     CUtensorMap tw_map;
     if (!tensor_map_u8_2d(&tw_map, w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, 224u)) return FQ_ERR_CUDA;
     debug_schedule("w8a8_quant_linear", M, K, N, mt, "dp224+quant", int(tiles));

@@ -21,6 +21,8 @@
 //    depend on timing) and store bf16 through a staging tile.
 // The scale chunks are the blocked layout quant_mxfp8 writes: for 128 rows x
 // 128 K, row r's byte for K block b at (r % 32) * 16 + ((r % 128) / 32) * 4 + b % 4.
+#include <cstdlib>
+
 #include "fq_common.cuh"
 
 namespace fq {
@@ -49,6 +51,7 @@ struct Cfg {
 
 struct Problem {
   int M, N, K, KB, m_tiles, n_tiles;
+  int ahead;  // stages kept in flight (<= the ring)
   int64_t total;
   const uint8_t* xsf;   // blocked token scales
   const uint8_t* wsf;   // blocked weight scales
@@ -152,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_it > 0) {
       const uint64_t pol_w = p.m_tiles > 1 ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      const int npre = n_it < S ? n_it : S;
+      const int AH = p.ahead < S ? p.ahead : S;
+      const int npre = n_it < AH ? n_it : AH;
       {  // weights and their scales do not depend on the previous kernel
         int tile = begin / KB, kb = begin - tile * KB;
         for (int r = 0; r < npre; ++r) {
@@ -174,7 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = r % S;
         uint8_t* st = smem + s * C::STAGE;
         if (r >= npre) {
-          if (s_abort || !mbar_wait(&empty[s], uint32_t((r / S - 1) & 1))) {
+          // iteration r - AH consumed: at most AH stages in flight, slot s free
+          const int rq = r - AH;
+          if (s_abort || !mbar_wait(&empty[rq % S], uint32_t((rq / S) & 1))) {
             if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
             s_abort = 1;
             break;
@@ -431,6 +437,12 @@ extern "C" __attribute__((visibility("default"))) fq_status mxfp8_linear(const u
     return FQ_ERR_CUDA;
   // at least 4 k-blocks per CTA: a CTA's fixed cost (pipeline fill, epilogue)
   // and a tile's stream-K hand-off grow with the number of CTAs sharing it
+  {  // stages in flight: about 120 KB per SM (see the W8A8 GEMM's stage cap)
+    const int stage = 128 * 128 + mt * 128 + 1024;
+    int ah = (122880 + stage / 2) / stage;
+    if (const char* v = std::getenv("FQ_STAGES_AHEAD")) ah = std::atoi(v);
+    p.ahead = ah < 2 ? 2 : ah;
+  }
   const int64_t by_work = (p.total + 3) / 4;
   const int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
   const bool pdl = pdl_enabled();
