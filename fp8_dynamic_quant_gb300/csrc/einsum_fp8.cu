@@ -608,6 +608,10 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   }
   const int64_t by_work = (p.total + 3) / 4;
   int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
+  {
+    const int g = whole_tile_grid(tiles, d.sm_count);
+    if (g > 0 && g <= grid) grid = g;
+  }
   if (const char* f = std::getenv("FQ_FORCE_SCHEDULE")) {
     if (!std::strcmp(f, "dp") && tiles <= es::kMaxGrid) grid = int(tiles);
     // each tile split in two halves (partial sums: the workspace holds two slots per SM)

@@ -422,4 +422,11 @@ fq_status quant_int8_launch(const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
                             bool trigger);
 size_t ws_mxfp8_linear(int64_t M, int64_t K, int64_t N);
 constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+// Stream-K grid that hands every CTA whole tiles when that still fills at
+// least 3/4 of the SMs: with ceil(tiles / sms) tiles a CTA, the CTA count is
+// ceil(tiles / that), and a tile count that it divides leaves no tile split
+// between CTAs - no partial sums, no hand-off at the end.  Returns 0 when the
+// whole-tile grid would leave more than a quarter of the SMs idle.  Env
+// FQ_WHOLE_TILES=0 turns it off (studies).
+int whole_tile_grid(int64_t tiles, int sms);
 }  // namespace fq

@@ -1688,7 +1688,11 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   // set-up, pipeline fill, epilogue - and a tile's hand-off grow with the CTAs
   // sharing the tile)
   const int64_t work = umma ? (p.total + 3) / 4 : p.total;
-  const int grid = data_parallel ? int(tiles) : int(work < d.sm_count ? (work > 0 ? work : 1) : d.sm_count);
+  int grid = data_parallel ? int(tiles) : int(work < d.sm_count ? (work > 0 ? work : 1) : d.sm_count);
+  if (umma) {
+    const int g = whole_tile_grid(tiles, d.sm_count);
+    if (g > 0 && g <= grid) grid = g;
+  }
   debug_schedule("w8a8_linear", M, K, N, mt_run, data_parallel ? "dp224" : (umma ? "umma" : "streamk"), grid);
   const bool pdl = pdl_enabled();
   cudaError_t e;

@@ -444,7 +444,11 @@ extern "C" __attribute__((visibility("default"))) fq_status mxfp8_linear(const u
     p.ahead = ah < 2 ? 2 : ah;
   }
   const int64_t by_work = (p.total + 3) / 4;
-  const int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
+  int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
+  {
+    const int g = whole_tile_grid(tiles, d.sm_count);
+    if (g > 0 && g <= grid) grid = g;
+  }
   const bool pdl = pdl_enabled();
   cudaError_t e;
   switch (mt) {

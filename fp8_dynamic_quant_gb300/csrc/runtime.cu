@@ -61,6 +61,16 @@ fq_status device_info(DevInfo* info) {
   return (d.major == 10 && d.minor == 3) ? FQ_OK : FQ_ERR_UNSUPPORTED_DEVICE;
 }
 
+int whole_tile_grid(int64_t tiles, int sms) {
+  const char* v = std::getenv("FQ_WHOLE_TILES");
+  if (v && v[0] == '0') return 0;
+  if (tiles <= 0 || sms <= 0) return 0;
+  const int64_t per = (tiles + sms - 1) / sms;
+  const int64_t g = (tiles + per - 1) / per;
+  if (tiles % g != 0) return 0;  // uneven: some tile would still be split
+  return g * 4 >= int64_t(sms) * 3 ? int(g) : 0;
+}
+
 bool pdl_enabled() {
   static int v = -1;
   if (v < 0) {
