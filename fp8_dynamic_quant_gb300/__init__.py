@@ -88,7 +88,13 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream():
+    """The current CUDA stream of the current device, as a raw handle."""
+    if _RAW_STREAM is not None:
+        return ctypes.c_void_p(_RAW_STREAM(torch.cuda.current_device()))
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
@@ -107,8 +113,18 @@ def _cuda(t, dtype, name):
     return t
 
 
+_WS_BYTES = {}
+
+
 def workspace_bytes(op, a, b=0, c=0, d=0):
-    return int(lib().fq_workspace_bytes(op, a, b, c, d))
+    """fq_workspace_bytes for the current device (memoised per device and arguments)."""
+    key = (torch.cuda.current_device() if torch.cuda.is_available() else -1, op, a, b, c, d)
+    v = _WS_BYTES.get(key)
+    if v is None:
+        v = int(lib().fq_workspace_bytes(op, a, b, c, d))
+        if v:
+            _WS_BYTES[key] = v
+    return v
 
 
 # Zero-filled workspaces, one per (device, stream); every call leaves them zero.
