@@ -43,7 +43,13 @@ constexpr int kBK = 128;
 constexpr int kMaxGrid = 1024;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-constexpr int kPre = 4;  // K blocks of scales in flight ahead of the promotion
+// K blocks of scales in flight ahead of the promotion.  A 4-byte load takes
+// about 2 us while the weight stream saturates HBM, so a shallow prefetch
+// paces the promotion: 4 blocks ahead held it to ~0.5 us per block on GB300.
+template <int MT>
+struct ScalePre {
+  static constexpr int value = MT > 32 ? 8 : 16;  // the ring of 64-token tiles must fit beside the stages
+};
 // K blocks per tensor-core commit.  A tcgen05.commit costs about a pipeline
 // drain (~0.3 us measured on GB300 for decode-sized MMAs, against ~25 ns per
 // 128x16x32 MMA when they stream), so stage release and the accumulator
@@ -75,31 +81,59 @@ struct GroupCursor {
     if (++kb == KB) kb = 0;
     ++r;
   }
+  // Chunk steps (KD blocks, KD dividing GROUP, KB and n_it; groups start at
+  // chunk starts, so no group ends inside a chunk): does the chunk at the
+  // cursor end its group, and the step past it.
+  __device__ __forceinline__ bool chunk_ends_group(int KD, int KB, int n_it) const {
+    return cnt + KD == GROUP || kb + KD == KB || r + KD == n_it;
+  }
+  __device__ __forceinline__ void advance_chunk(int KD, int KB, int n_it) {
+    if (chunk_ends_group(KD, KB, n_it)) {
+      ++g;
+      cnt = 0;
+    } else {
+      cnt += KD;
+    }
+    kb += KD;
+    if (kb == KB) kb = 0;
+    r += KD;
+  }
 };
 
-template <int MT>
+// BM weight rows per tile: 128 (tcgen05 M = 128) or 64 (M = 64; the
+// accumulator's row r then sits in tensor-memory lane 32 * (r / 16) + r % 16,
+// the first 16 lanes of each warp's quarter).
+template <int MT, int BM>
 struct Cfg {
-  static constexpr int W_BYTES = 128 * kBK;
-  static constexpr int X_BYTES = MT * kBK;
-  static constexpr int STAGE = W_BYTES + X_BYTES;  // multiple of 1024
-  // ~200 KB of weights in flight per SM to cover loaded HBM latency (half
-  // that, to fit two CTAs per SM, measured slower: 17.5 against 15 us at T=1)
-  static constexpr int STAGES_FIT = (208 * 1024) / STAGE;
-  static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
+  static constexpr int W_SUB = BM * kBK;  // one K block of the weight tile (multiple of 1024)
+  static constexpr int X_SUB = MT * kBK;  // one K block of the token tile (multiple of 1024)
   static constexpr int GROUP = GroupSize<MT>::value;
   static constexpr int NACC = 2 * GROUP;           // accumulator slots: two groups of K blocks
   static constexpr uint32_t TMEM_COLS = NACC * MT <= 128 ? 128u : (NACC * MT <= 256 ? 256u : 512u);
-  static constexpr int SLOT = 128 * MT;             // fp32 per partial-sum slot
-  static constexpr int SMEM = STAGES * STAGE + (STAGES + kGroupBars + 2 + 1) * 8 + 1024;
-  static_assert(STAGES >= 4, "pipeline too shallow");
+  static constexpr int SLOT = BM * MT;              // fp32 per partial-sum slot
   static_assert(NACC * MT <= 512, "tensor-memory budget");
-  static_assert(kGroupBars > STAGES, "group barriers must outnumber the stages (no parity aliasing)");
+  static_assert(GROUP % 4 == 0, "a commit group holds whole stages (KD divides 4)");
 };
+// A stage holds KD consecutive K blocks (1, 2 or 4) of one tile: KD weight
+// sub-tiles, then KD token sub-tiles, each fetched by one 3-D TMA box.  TMA
+// throughput per SM is set by the number of copies more than by their bytes
+// (measured on GB300 with one CTA per SM streaming 256 MB: 8 KB boxes 3.3 TB/s,
+// 16 KB 6.0, 32-64 KB 6.2-6.4), so small tiles fetch several K blocks at once.
+constexpr int kStageBudget = 208 * 1024;  // ~200 KB of stages in flight per SM
+constexpr int kMaxStages = 16;
+constexpr int kMinStages = 4;
+static_assert(kGroupBars > kMaxStages, "group barriers must outnumber the stages (no parity aliasing)");
+__host__ __device__ constexpr int stage_bytes(int KD, int BM, int MT) { return KD * (BM + MT) * kBK; }
+__host__ __device__ constexpr int smem_bytes(int S, int stage) { return S * stage + (S + kGroupBars + 3) * 8 + 1024; }
 
 struct Problem {
   int T, G, D, N, KB, NB, TT, P, Ta;
-  int ahead;  // stages kept in flight (<= the ring)
-  int64_t total;
+  int NS;     // weight-scale blocks along N (N / 128); NB counts tiles of BM rows
+  int KD;     // K blocks per stage (divides KB)
+  int S;      // stages in the ring
+  int stage;  // bytes per stage
+  int ahead;  // stages kept in flight (<= S)
+  int64_t total;  // stream-K units: (tile, chunk of KD K blocks) pairs
   const void* sx;
   const float* sw;
   uint16_t* y;
@@ -108,14 +142,27 @@ struct Problem {
   uint32_t* err;
 };
 
-// First iteration of CTA c's stream-K range: floor(c * total / G).
-__device__ __forceinline__ int range_begin(int64_t total, int G, int c) { return int(int64_t(c) * total / G); }
-// CTA whose stream-K range holds iteration i: the largest c with range_begin(c) <= i.
-__device__ __forceinline__ int cta_of(int64_t total, int G, int i) {
+// Wait that reads the CTA's abort flag only once the phase is found
+// incomplete: a shared-memory flag read per K block cost the single-thread
+// issue loop ~60 ns on GB300.
+static __device__ __noinline__ bool wait_slow_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return !*abort_flag && mbar_wait_slow(bar, parity, kWaitNs);
+}
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || wait_slow_or_abort(bar, parity, abort_flag);
+}
+
+// First K-block iteration of CTA c's stream-K range: the ranges split the
+// (tile, chunk) units evenly, floor(c * total / G) chunks of KD blocks each.
+__device__ __forceinline__ int range_begin(const Problem& p, int G, int c) {
+  return int(int64_t(c) * p.total / G) * p.KD;
+}
+// CTA whose stream-K range holds K-block iteration i: the largest c with range_begin(c) <= i.
+__device__ __forceinline__ int cta_of(const Problem& p, int G, int i) {
   int lo = 0, hi = G;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (range_begin(total, G, mid) <= i) lo = mid; else hi = mid;
+    if (range_begin(p, G, mid) <= i) lo = mid; else hi = mid;
   }
   return lo;
 }
@@ -174,23 +221,25 @@ __host__ __device__ constexpr uint32_t idesc_f8(int M, int N) {
   return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-template <int MT, int FMT>
+template <int MT, int FMT, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_einsum_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, Problem p) {
-  using C = Cfg<MT>;
-  constexpr int S = C::STAGES, NACC = C::NACC, kEpi = kEpiWarps * 32;
+  using C = Cfg<MT, BM>;
+  constexpr int kEpi = kEpiWarps * 32;
+  const int S = p.S, KD = p.KD, STAGE = p.stage;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * STAGE);
   uint64_t* grp = full + S;                 // [kGroupBars]: the MMAs of group g have completed
   uint64_t* acc_empty = grp + kGroupBars;   // [2]: the epilogue has drained group g's slots
   uint64_t* done_bar = acc_empty + 2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_flag, s_issued, s_consumed;
   __shared__ volatile int s_abort;
-  __shared__ __align__(16) float s_f[kEpiWarps][MT];        // per-token scale factors of the current block
+  __shared__ __align__(16) float s_f[kEpiWarps][4 * MT];    // per-token scale factors of the current chunk
+  constexpr int kPre = ScalePre<MT>::value;
   __shared__ __align__(16) uint32_t s_ring[kEpiWarps][kPre * (MT + 4)];  // scale words, kPre blocks ahead
-  __shared__ __align__(16) uint16_t s_ystage[16 * 128];
+  __shared__ __align__(16) uint16_t s_ystage[16 * BM];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, b = blockIdx.x;
@@ -207,15 +256,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
     // weights do not depend on the previous kernel: the first stages go out now
-    const int b0 = int(int64_t(b) * p.total / G), b1 = int(int64_t(b + 1) * p.total / G);
-    npre = min(b1 - b0, p.ahead);
+    const int b0 = range_begin(p, G, b), b1 = range_begin(p, G, b + 1);
+    npre = min((b1 - b0) / KD, p.ahead);
     const uint64_t pol_w = p.TT > 1 ? policy_evict_normal() : policy_evict_first();
     int tile = b0 / p.KB, kb = b0 - tile * p.KB;
     ETile t = etile(p, tile);
-    for (int r = 0; r < npre; ++r) {
-      mbar_arrive_expect_tx(&full[r], C::STAGE);
-      tma_load_2d(smem + r * C::STAGE, &tmW, &full[r], kb * kBK, t.g * p.N + t.nb * 128, pol_w);
-      if (++kb == p.KB && r + 1 < npre) {
+    for (int q = 0; q < npre; ++q) {
+      mbar_arrive_expect_tx(&full[q], STAGE);
+      tma_load_3d(smem + q * STAGE, &tmW, &full[q], 0, t.g * p.N + t.nb * BM, kb, pol_w);
+      kb += KD;
+      if (kb == p.KB && q + 1 < npre) {
         kb = 0;
         t = etile(p, ++tile);
       }
@@ -229,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int begin = range_begin(p.total, G, b), end = range_begin(p.total, G, b + 1), n_it = end - begin;
+  const int begin = range_begin(p, G, b), end = range_begin(p, G, b + 1), n_it = end - begin;
   const int KB = p.KB;
 
   if (warp == 0) {
@@ -241,27 +291,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tile = begin / KB, kb = begin - tile * KB;
       ETile t = etile(p, tile);
       int issued = 0;
-      GroupCursor<C::GROUP> lag;  // the iteration that last used the stage being refilled
+      GroupCursor<C::GROUP> lag;  // at chunk q - ahead, whose group gates the refill
       lag.kb = kb;
-      for (int r = 0; r < n_it; ++r) {
-        const int s = r % S;
-        uint8_t* st = smem + s * C::STAGE;
-        if (r >= npre) {
-          // iteration r - ahead's group completed: at most `ahead` stages in
-          // flight, and (r - S <= r - ahead) slot s is free
+      const int nq = n_it / KD;
+      for (int q = 0, s = 0; q < nq; ++q) {
+        uint8_t* st = smem + s * STAGE;
+        if (q >= npre) {
+          // the group holding chunk q - ahead completed: at most `ahead`
+          // stages in flight, and (q - S <= q - ahead) stage s is free
+          if (q > p.ahead) lag.advance_chunk(KD, KB, n_it);
           const int gl = lag.g;
-          lag.advance(KB, n_it);
-          if (s_abort || !mbar_wait(&grp[gl % kGroupBars], uint32_t((gl / kGroupBars) & 1))) {
+          if (!wait_or_abort(&grp[gl % kGroupBars], uint32_t((gl / kGroupBars) & 1), &s_abort)) {
             if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
             s_abort = 1;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], C::STAGE);
-          tma_load_2d(st, &tmW, &full[s], kb * kBK, t.g * p.N + t.nb * 128, pol_w);
+          mbar_arrive_expect_tx(&full[s], STAGE);
+          tma_load_3d(st, &tmW, &full[s], 0, t.g * p.N + t.nb * BM, kb, pol_w);
         }
-        tma_load_2d(st + C::W_BYTES, &tmX, &full[s], t.g * p.D + kb * kBK, t.tt * MT, pol_x);
+        tma_load_3d(st + KD * C::W_SUB, &tmX, &full[s], 0, t.tt * MT, t.g * KB + kb, pol_x);
         ++issued;
-        if (++kb == KB && r + 1 < n_it) {
+        if (++s == S) s = 0;
+        kb += KD;
+        if (kb == KB && q + 1 < nq) {
           kb = 0;
           t = etile(p, ++tile);
         }
@@ -270,46 +322,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      // The issuing thread's own instruction stream is on the critical path
-      // (one thread, dependent integer work between MMAs), so descriptors are
-      // formed once and advanced by adding the address offset (in 16-byte
-      // units) to their low field, and the stage / phase counters step
-      // incrementally.
-      const uint64_t da0 = umma_desc_k_sw128(smem_u32(smem));
-      const uint64_t db0 = umma_desc_k_sw128(smem_u32(smem) + C::W_BYTES);
-      constexpr uint32_t idesc = idesc_f8(128, MT);
-      int consumed = 0, s = 0;
-      uint32_t phase = 0;
-      GroupCursor<C::GROUP> cur;
-      cur.kb = begin % KB;
-      for (int r = 0; r < n_it; ++r) {
-        bool ok = !s_abort;
-        // a group reuses the slots of the group two back: wait until the epilogue drained it
-        if (ok && cur.cnt == 0 && cur.g >= 2)
-          ok = mbar_wait(&acc_empty[cur.g & 1], uint32_t(((cur.g >> 1) - 1) & 1));
-        if (ok) ok = mbar_wait(&full[s], phase);
-        if (!ok) {
+    // The whole warp walks the chunks (waits and loop control warp-uniform)
+    // and one elected lane issues a chunk's KD x 4 MMAs as one straight
+    // sequence from a base descriptor plus constant offsets (16-byte units in
+    // the low field).  Measured on GB300 with decode-sized MMAs: ~30 ns per
+    // MMA this way, against ~110 ns when one thread issued block by block
+    // with a wait between blocks.
+    const uint64_t da0 = umma_desc_k_sw128(smem_u32(smem));
+    const uint64_t db0 = umma_desc_k_sw128(smem_u32(smem) + uint32_t(KD * C::W_SUB));
+    constexpr uint32_t idesc = idesc_f8(BM, MT);
+    int consumed = 0, s = 0;
+    uint32_t phase = 0;
+    GroupCursor<C::GROUP> cur;
+    cur.kb = begin % KB;
+    const int nq = n_it / KD;
+    for (int qi = 0; qi < nq; ++qi) {
+      bool ok = true;
+      // a group starts with this chunk and reuses the slots of the group two back
+      if (cur.cnt == 0 && cur.g >= 2)
+        ok = wait_or_abort(&acc_empty[cur.g & 1], uint32_t(((cur.g >> 1) - 1) & 1), &s_abort);
+      if (ok) ok = wait_or_abort(&full[s], phase, &s_abort);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) {
+        if (lane == 0) {
           if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
           s_abort = 1;
-          break;
         }
-        tc_fence_after();
-        const uint64_t off = uint64_t(uint32_t(s * C::STAGE) >> 4);
-        const uint32_t d = tmem + uint32_t(((cur.g & 1) * C::GROUP + cur.cnt) * MT);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) umma_f8(d, da0 + off + uint64_t(2 * j), db0 + off + uint64_t(2 * j), idesc, j > 0 ? 1u : 0u);
-        // one commit per group: releases the group's stages and hands its slots to the epilogue
-        if (cur.group_end(KB, n_it)) umma_commit(&grp[cur.g % kGroupBars]);
-        cur.advance(KB, n_it);
-        ++consumed;
-        if (++s == S) {
-          s = 0;
-          phase ^= 1u;
-        }
+        break;
       }
-      umma_commit(done_bar);
-      if (!mbar_wait(done_bar, 0)) atomicOr(p.err, DEVERR_TIMEOUT);
+      tc_fence_after();
+      const uint64_t so = uint64_t(uint32_t(s * STAGE) >> 4);
+      const uint64_t da = da0 + so, db = db0 + so;
+      const uint32_t d = tmem + uint32_t(((cur.g & 1) * C::GROUP + cur.cnt) * MT);
+      const bool gend = cur.chunk_ends_group(KD, KB, n_it);
+      if (elect_one()) {
+#pragma unroll
+        for (int kd = 0; kd < 4; ++kd) {
+          if (kd < KD) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              umma_f8(d + uint32_t(kd * MT), da + uint64_t((kd * C::W_SUB) >> 4) + uint64_t(2 * j),
+                      db + uint64_t((kd * C::X_SUB) >> 4) + uint64_t(2 * j), idesc, j > 0 ? 1u : 0u);
+          }
+        }
+        // one commit per group: releases the group's stages and hands its slots to the epilogue
+        if (gend) umma_commit(&grp[cur.g % kGroupBars]);
+      }
+      __syncwarp();
+      cur.advance_chunk(KD, KB, n_it);
+      ++consumed;
+      if (++s == S) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+    if (elect_one()) umma_commit(done_bar);
+    __syncwarp();
+    const bool dok = mbar_wait(done_bar, 0);
+    if (lane == 0) {
+      if (!dok) atomicOr(p.err, DEVERR_TIMEOUT);
       s_consumed = consumed;  // stages whose copies are known to have landed
     }
     __syncwarp();
@@ -320,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dependent may prefetch weights before its own wait, which is safe only
     // if every earlier kernel has finished.
     pdl_launch_dependents();
-    const int q = warp & 3, nl = 32 * q + lane, etid = tid - 64;
+    // this thread's weight row of the tile (BM = 64: lanes 0-15 of each quarter)
+    const int q = warp & 3, etid = tid - 64;
+    const bool rowv = BM == 128 || lane < 16;
+    const int nl = BM == 128 ? 32 * q + lane : 16 * q + (lane & 15);
     const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
     float* sf = s_f[warp - 2];
     float acc[MT];
@@ -330,65 +404,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     ETile t = etile(p, tile);
     bool first_seg = true;
     // Scales stream through a per-warp ring in shared memory, kPre blocks
-    // ahead, by asynchronous 4-byte copies (lane j copies token j's stored
-    // word, and j + 32's; lane 0 the weight-block scale): a block's promotion
-    // never waits on a global round trip.  Slot layout: MT token words, then sw.
+    // (kPre / 4 chunks) ahead, by asynchronous 4-byte copies (lane j copies
+    // token j's stored word, and j + 32's; lane 0 the weight-block scale): a
+    // block's promotion never waits on a global round trip.  Chunk slot: four
+    // block slots of MT token words, then sw.
     constexpr int TPL = MT > 32 ? 2 : 1;
+    constexpr int kSlotW = MT + 4, kPreC = kPre / 4;
     uint32_t* ring = s_ring[warp - 2];
-    int tile_p = tile, kb_p = kb;  // block of the next copy to issue
-    auto issue = [&](int it) {
-      const ETile tp = etile(p, tile_p);
-      uint32_t* slot = ring + (it % kPre) * (MT + 4);
+    int tile_p = tile, kb_p = kb;  // first block of the next chunk to fetch
+    auto issue = [&](int qq) {
+      const ETile tp = etile(p, tile_p);  // a chunk lies in one tile
+      uint32_t* cs = ring + (qq % kPreC) * (4 * kSlotW);
+      for (int kd = 0; kd < KD; ++kd) {
+        uint32_t* slot = cs + kd * kSlotW;
+        const int kbb = kb_p + kd;
 #pragma unroll
-      for (int i = 0; i < TPL; ++i) {
-        const int m = lane + 32 * i, tok = tp.tt * MT + m;
-        if (m < MT && tok < p.T) {
-          const void* src = FMT == FQ_SCALE_UE8M0_PACKED
-                                ? static_cast<const void*>(static_cast<const uint32_t*>(p.sx) +
-                                                           (int64_t(tp.g) * p.P + (kb_p >> 2)) * p.Ta + tok)
-                                : static_cast<const void*>(static_cast<const float*>(p.sx) +
-                                                           (int64_t(tok) * p.G + tp.g) * KB + kb_p);
-          cp_async4(slot + m, src);
+        for (int i = 0; i < TPL; ++i) {
+          const int m = lane + 32 * i, tok = tp.tt * MT + m;
+          if (m < MT && tok < p.T) {
+            const void* src = FMT == FQ_SCALE_UE8M0_PACKED
+                                  ? static_cast<const void*>(static_cast<const uint32_t*>(p.sx) +
+                                                             (int64_t(tp.g) * p.P + (kbb >> 2)) * p.Ta + tok)
+                                  : static_cast<const void*>(static_cast<const float*>(p.sx) +
+                                                             (int64_t(tok) * p.G + tp.g) * KB + kbb);
+            cp_async4(slot + m, src);
+          }
         }
+        if (lane == 0) cp_async4(slot + MT, p.sw + (int64_t(tp.g) * KB + kbb) * p.NS + (tp.nb * BM) / 128);
       }
-      if (lane == 0) cp_async4(slot + MT, p.sw + (int64_t(tp.g) * KB + kb_p) * p.NB + tp.nb);
-      if (++kb_p == KB) {
+      kb_p += KD;
+      if (kb_p == KB) {
         kb_p = 0;
         ++tile_p;
       }
     };
+    const int nq = n_it / KD;
 #pragma unroll 1
-    for (int it = 0; it < kPre; ++it) {
-      if (it < n_it) issue(it);
+    for (int it = 0; it < kPreC; ++it) {
+      if (it < nq) issue(it);
       cp_async_commit();
     }
+    // tensor-memory loads in flight at once: 64 registers' worth of blocks
+    constexpr int LB = 64 / MT;
     GroupCursor<C::GROUP> ec;
     ec.kb = kb;
     bool gok = true;
-    for (int r = 0; r < n_it; ++r) {
-      const bool seg_end = (kb == KB - 1) || (r == n_it - 1);
-      // this block's per-token factors sx[t] * sw (0 past T), through shared memory
-      cp_async_wait<kPre - 1>();
+    for (int qi = 0; qi < nq; ++qi) {
+      const bool seg_end = (kb + KD == KB) || (qi == nq - 1);
+      // the chunk's per-token factors sx[t] * sw (0 past T), through shared memory
+      cp_async_wait<kPreC - 1>();
       __syncwarp();
       {
-        const uint32_t* slot = ring + (r % kPre) * (MT + 4);
-        const float swv = __uint_as_float(slot[MT]);
-        float fv[TPL];
+        const uint32_t* cs = ring + (qi % kPreC) * (4 * kSlotW);
+        float fv[4][TPL];
 #pragma unroll
-        for (int i = 0; i < TPL; ++i) {
-          const int m = lane + 32 * i;
-          fv[i] = (m < MT && t.tt * MT + m < p.T) ? __fmul_rn(decode_sx<FMT>(slot[m], kb), swv) : 0.0f;
+        for (int kd = 0; kd < 4; ++kd) {
+          if (kd < KD) {
+            const uint32_t* slot = cs + kd * kSlotW;
+            const float swv = __uint_as_float(slot[MT]);
+#pragma unroll
+            for (int i = 0; i < TPL; ++i) {
+              const int m = lane + 32 * i;
+              fv[kd][i] = (m < MT && t.tt * MT + m < p.T) ? __fmul_rn(decode_sx<FMT>(slot[m], kb + kd), swv) : 0.0f;
+            }
+          }
         }
-        __syncwarp();  // the slot is read; its next copy may go out
+        __syncwarp();  // the slots are read; their next copies may go out
 #pragma unroll
-        for (int i = 0; i < TPL; ++i)
-          if (lane + 32 * i < MT) sf[lane + 32 * i] = fv[i];
+        for (int kd = 0; kd < 4; ++kd) {
+          if (kd < KD) {
+#pragma unroll
+            for (int i = 0; i < TPL; ++i)
+              if (lane + 32 * i < MT) sf[kd * MT + lane + 32 * i] = fv[kd][i];
+          }
+        }
       }
-      if (r + kPre < n_it) issue(r + kPre);
+      if (qi + kPreC < nq) issue(qi + kPreC);
       cp_async_commit();
       __syncwarp();
       if (ec.cnt == 0) {  // a group starts: wait once for all of its MMAs
-        gok = !s_abort && mbar_wait(&grp[ec.g % kGroupBars], uint32_t((ec.g / kGroupBars) & 1));
+        gok = wait_or_abort(&grp[ec.g % kGroupBars], uint32_t((ec.g / kGroupBars) & 1), &s_abort);
         gok = __all_sync(0xFFFFFFFFu, gok);
         if (!gok) {
           if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
@@ -397,45 +492,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       const bool ok = gok;
-      const uint32_t acol = uint32_t(((ec.g & 1) * C::GROUP + ec.cnt) * MT);
       if (ok) {
-        // 16 columns at a time: load, wait, promote (keeps the registers of
-        // one chunk, not of the whole tile, in flight)
+        // up to LB blocks' accumulators loaded together, one wait, then
+        // promoted in order: acc += blk * f
 #pragma unroll
-        for (int h = 0; h < MT / 16; ++h) {
-          uint32_t v[16];
-          tmem_ld16(trow + acol + uint32_t(16 * h), v);
-          tmem_wait_ld();
+        for (int kd0 = 0; kd0 < 4; kd0 += LB) {
+          if (kd0 < KD) {
+            uint32_t v[LB][MT / 16][16];
 #pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const float4 f = *reinterpret_cast<const float4*>(sf + 16 * h + 4 * j4);
-            float* a4 = acc + 16 * h + 4 * j4;
-            a4[0] = __fmaf_rn(__uint_as_float(v[4 * j4 + 0]), f.x, a4[0]);
-            a4[1] = __fmaf_rn(__uint_as_float(v[4 * j4 + 1]), f.y, a4[1]);
-            a4[2] = __fmaf_rn(__uint_as_float(v[4 * j4 + 2]), f.z, a4[2]);
-            a4[3] = __fmaf_rn(__uint_as_float(v[4 * j4 + 3]), f.w, a4[3]);
+            for (int u = 0; u < LB; ++u) {
+              if (kd0 + u < KD) {
+                const uint32_t acol = uint32_t(((ec.g & 1) * C::GROUP + ec.cnt + kd0 + u) * MT);
+#pragma unroll
+                for (int h = 0; h < MT / 16; ++h) tmem_ld16(trow + acol + uint32_t(16 * h), v[u][h]);
+              }
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < LB; ++u) {
+              if (kd0 + u < KD) {
+                const float* fk = sf + (kd0 + u) * MT;
+#pragma unroll
+                for (int j4 = 0; j4 < MT / 4; ++j4) {
+                  const float4 f = *reinterpret_cast<const float4*>(fk + 4 * j4);
+                  float* a4 = acc + 4 * j4;
+                  const uint32_t* v4 = &v[u][j4 >> 2][4 * (j4 & 3)];
+                  a4[0] = __fmaf_rn(__uint_as_float(v4[0]), f.x, a4[0]);
+                  a4[1] = __fmaf_rn(__uint_as_float(v4[1]), f.y, a4[1]);
+                  a4[2] = __fmaf_rn(__uint_as_float(v4[2]), f.z, a4[2]);
+                  a4[3] = __fmaf_rn(__uint_as_float(v4[3]), f.w, a4[3]);
+                }
+              }
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      // the group's last block is read: its slots may take the group after next
-      if (ec.group_end(KB, n_it) && lane == 0 && ok) mbar_arrive(&acc_empty[ec.g & 1]);
-      ec.advance(KB, n_it);
-      __syncwarp();  // sf is rewritten for the next block
+      // the group's last chunk is read: its slots may take the group after next
+      if (ec.chunk_ends_group(KD, KB, n_it) && lane == 0 && ok) mbar_arrive(&acc_empty[ec.g & 1]);
+      ec.advance_chunk(KD, KB, n_it);
+      __syncwarp();  // sf is rewritten for the next chunk
       if (seg_end) {
-        // ---- segment end: tile `tile`, K blocks [seg_kb0, kb]
-        const int n0 = t.nb * 128, m0 = t.tt * MT;
+        // ---- segment end: tile `tile`, K blocks [seg_kb0, kb + KD - 1]
+        const int n0 = t.nb * BM, m0 = t.tt * MT;
         const int rows = min(MT, p.T - m0);
-        const bool whole = (seg_kb0 == 0) && (kb == KB - 1);
+        const bool whole = (seg_kb0 == 0) && (kb + KD == KB);
         if (!whole) {
-          // this CTA's partial sums -> its slot [MT tokens][128 rows]
+          // this CTA's partial sums -> its slot [MT tokens][BM rows]
           float* my = p.slots + (2 * int64_t(b) + (first_seg ? 0 : 1)) * C::SLOT + nl;
+          if (rowv) {
 #pragma unroll
-          for (int j = 0; j < MT; ++j) my[j * 128] = acc[j];
+            for (int j = 0; j < MT; ++j) my[j * BM] = acc[j];
+          }
           named_bar_sync(1, kEpi);
           if (etid == 0) {
-            const uint32_t nbk = uint32_t(kb - seg_kb0 + 1);
+            const uint32_t nbk = uint32_t(kb + KD - seg_kb0);
             const uint32_t old = atom_add_acq_rel_gpu(&p.counters[tile], nbk);
             const int last = (old + nbk == uint32_t(KB)) ? 1 : 0;
             if (last) p.counters[tile] = 0;  // every contributor has arrived; ready for the next call
@@ -448,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!whole) {
             // every contributor's slot, this CTA's own included, added in
             // ascending CTA order; four contributors' loads in flight at once
-            const int c0 = cta_of(p.total, G, tile * KB), c1 = cta_of(p.total, G, tile * KB + KB - 1);
+            const int c0 = cta_of(p, G, tile * KB), c1 = cta_of(p, G, tile * KB + KB - 1);
 #pragma unroll
             for (int j = 0; j < MT; ++j) acc[j] = 0.0f;
             for (int cb = c0; cb <= c1; cb += 4) {
@@ -458,17 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                   const int cc = cb + u;
-                  const int cb0 = range_begin(p.total, G, cc);
-                  const bool use = cc <= c1 && range_begin(p.total, G, cc + 1) != cb0;
+                  const int cb0 = range_begin(p, G, cc);
+                  const bool use = cc <= c1 && range_begin(p, G, cc + 1) != cb0;
                   const int first_tile = use ? cb0 / KB : tile;
                   const float* sl = p.slots + (2 * int64_t(use ? cc : b) + (first_tile == tile ? 0 : 1)) * C::SLOT +
-                                    nl + 16 * h * 128;
+                                    nl + 16 * h * BM;
 #pragma unroll
-                  for (int j = 0; j < 16; ++j) vv[u][j] = use ? __ldcg(sl + j * 128) : 0.0f;
+                  for (int j = 0; j < 16; ++j) vv[u][j] = (use && rowv) ? __ldcg(sl + j * BM) : 0.0f;
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                  if (cb + u <= c1 && range_begin(p.total, G, cb + u + 1) != range_begin(p.total, G, cb + u)) {
+                  if (cb + u <= c1 && range_begin(p, G, cb + u + 1) != range_begin(p, G, cb + u)) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[16 * h + j] = __fadd_rn(acc[16 * h + j], vv[u][j]);
                   }
@@ -478,16 +590,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           // bf16 through a staging tile, 16 tokens at a time, 16-byte stores
 #pragma unroll
           for (int h = 0; h < MT / 16; ++h) {
+            if (rowv) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) s_ystage[j * 128 + nl] = f32_to_bf16_bits(acc[16 * h + j]);
+              for (int j = 0; j < 16; ++j) s_ystage[j * BM + nl] = f32_to_bf16_bits(acc[16 * h + j]);
+            }
             named_bar_sync(1, kEpi);
+            // 16 tokens x BM / 8 chunks of 8 outputs: one or two 16-byte stores a thread
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int piece = i * kEpi + etid, j = piece >> 4, c8 = piece & 15;
+            for (int i = 0; i < BM / 64; ++i) {
+              const int piece = i * kEpi + etid, j = piece / (BM / 8), c8 = piece % (BM / 8);
               const int m = 16 * h + j;
               if (m < rows)
                 st_global_v4(p.y + (int64_t(m0 + m) * p.G + t.g) * p.N + n0 + 8 * c8,
-                             *reinterpret_cast<const uint4*>(&s_ystage[j * 128 + 8 * c8]));
+                             *reinterpret_cast<const uint4*>(&s_ystage[j * BM + 8 * c8]));
             }
             named_bar_sync(1, kEpi);
           }
@@ -498,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_seg = false;
         seg_kb0 = 0;
       }
-      if (++kb == KB) {
+      kb += KD;
+      if (kb == KB) {
         kb = 0;
         t = etile(p, ++tile);
       }
@@ -516,27 +632,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int pick_mt(int64_t T) { return T <= 16 ? 16 : (T <= 32 ? 32 : 64); }
 
-template <int MT, int FMT>
+template <int MT, int FMT, int BM>
 cudaError_t launch_es1(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int grid, cudaStream_t s,
                        bool pdl) {
-  using Cf = Cfg<MT>;
-  auto k = fp8_einsum_kernel<MT, FMT>;
+  auto k = fp8_einsum_kernel<MT, FMT, BM>;
   static uint64_t attr_done = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(attr_done & (1ull << (dev & 63)))) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes(kMaxStages, kStageBudget / kMaxStages));
     if (e != cudaSuccess) return e;
     attr_done |= 1ull << (dev & 63);
   }
-  return launch(k, dim3(grid), dim3(kThreads), size_t(Cf::SMEM), s, pdl, *tw, *tx, p);
+  return launch(k, dim3(grid), dim3(kThreads), size_t(smem_bytes(p.S, p.stage)), s, pdl, *tw, *tx, p);
 }
 // The scale format is a compile-time parameter of the kernel.
 template <int MT>
-cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int fmt, int grid,
+cudaError_t launch_es(const CUtensorMap* tw, const CUtensorMap* tx, const Problem& p, int fmt, int bm, int grid,
                       cudaStream_t s, bool pdl) {
-  return fmt == FQ_SCALE_UE8M0_PACKED ? launch_es1<MT, FQ_SCALE_UE8M0_PACKED>(tw, tx, p, grid, s, pdl)
-                                      : launch_es1<MT, FQ_SCALE_FP32>(tw, tx, p, grid, s, pdl);
+  if (bm == 64)
+    return fmt == FQ_SCALE_UE8M0_PACKED ? launch_es1<MT, FQ_SCALE_UE8M0_PACKED, 64>(tw, tx, p, grid, s, pdl)
+                                        : launch_es1<MT, FQ_SCALE_FP32, 64>(tw, tx, p, grid, s, pdl);
+  return fmt == FQ_SCALE_UE8M0_PACKED ? launch_es1<MT, FQ_SCALE_UE8M0_PACKED, 128>(tw, tx, p, grid, s, pdl)
+                                      : launch_es1<MT, FQ_SCALE_FP32, 128>(tw, tx, p, grid, s, pdl);
 }
 }  // namespace es
 
@@ -574,13 +693,39 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   p.D = int(D);
   p.N = int(N);
   p.KB = int(D / 128);
-  p.NB = int(N / 128);
+  p.NS = int(N / 128);
   p.TT = int((T + mt - 1) / mt);
   p.P = int((D / 128 + 3) / 4);
   p.Ta = int((T + 3) / 4 * 4);
+  // Tile rows: 128 when whole 128-row tiles fill the SMs; else 64-row tiles
+  // (M = 64 MMAs, half the weight bytes per CTA) when those do - whole tiles
+  // need no partial-sum hand-off; else 128-row tiles under stream-K.
+  int bm = 128;
+  {
+    const int64_t t128 = G * int64_t(p.NS) * p.TT;
+    if (whole_tile_grid(t128, d.sm_count) <= 0 && whole_tile_grid(2 * t128, d.sm_count) > 0) bm = 64;
+    if (const char* v = std::getenv("FQ_EINSUM_BM")) bm = std::atoi(v) == 64 ? 64 : 128;
+  }
+  p.NB = int(N / bm);
+  // K blocks per stage: the most of 4, 2, 1 that divides KB and leaves at
+  // least kMinStages stages (FQ_EINSUM_KD = 1 | 2 | 4 fixes it for tests)
+  {
+    int kd = 4;
+    while (kd > 1 && (p.KB % kd || es::kStageBudget / es::stage_bytes(kd, bm, mt) < es::kMinStages)) kd >>= 1;
+    if (const char* v = std::getenv("FQ_EINSUM_KD")) {
+      const int f = std::atoi(v);
+      if ((f == 1 || f == 2 || f == 4) && p.KB % f == 0 &&
+          es::kStageBudget / es::stage_bytes(f, bm, mt) >= es::kMinStages)
+        kd = f;
+    }
+    p.KD = kd;
+    p.stage = es::stage_bytes(kd, bm, mt);
+    const int fit = es::kStageBudget / p.stage;
+    p.S = fit > es::kMaxStages ? es::kMaxStages : fit;
+  }
   const int64_t tiles = G * p.NB * int64_t(p.TT);
   if (tiles > kMaxTiles || tiles * p.KB > (int64_t(1) << 30)) return FQ_ERR_SHAPE;
-  p.total = tiles * p.KB;
+  p.total = tiles * (p.KB / p.KD);
   const size_t need = kCounterBytes + size_t(2) * d.sm_count * 128 * mt * 4;
   if (!ws || ws_bytes < need) return FQ_ERR_WORKSPACE;
   if (!aligned16(ws)) return FQ_ERR_ALIGN;
@@ -590,41 +735,50 @@ extern "C" __attribute__((visibility("default"))) fq_status fp8_group_einsum(con
   p.counters = static_cast<uint32_t*>(ws);
   p.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kCounterBytes);
   p.err = d.err_word;
+  // 3-D views (128 bytes of a K block, rows, K blocks): W [G*N rows][KB] and
+  // xq [T rows][G*KB]; one box is KD K blocks of a row tile.
   CUtensorMap tw_map, tx_map;
-  if (!tensor_map_u8_2d(&tw_map, w_gnd, uint64_t(D), uint64_t(G * N), uint64_t(D), es::kBK, 128u) ||
-      !tensor_map_u8_2d(&tx_map, xq, uint64_t(G * D), uint64_t(T), uint64_t(G * D), es::kBK, uint32_t(mt)))
-    return FQ_ERR_CUDA;
-  // Schedule: stream-K over one CTA per SM, at least 4 K blocks per CTA (a
-  // CTA's fixed cost - tensor-memory set-up, pipeline fill, hand-off - grows
-  // with the number of CTAs sharing a tile).  FQ_FORCE_SCHEDULE=dp gives every
-  // CTA one whole tile instead (no partial sums; tests and studies).
+  {
+    const uint64_t wd[3] = {uint64_t(es::kBK), uint64_t(G * N), uint64_t(p.KB)}, wst[2] = {uint64_t(D), 128u};
+    const uint64_t xd[3] = {uint64_t(es::kBK), uint64_t(T), uint64_t(G * p.KB)}, xs[2] = {uint64_t(G * D), 128u};
+    const uint32_t wb[3] = {uint32_t(es::kBK), uint32_t(bm), uint32_t(p.KD)};
+    const uint32_t xb[3] = {uint32_t(es::kBK), uint32_t(mt), uint32_t(p.KD)};
+    if (!tensor_map_u8_3d(&tw_map, w_gnd, wd, wst, wb) || !tensor_map_u8_3d(&tx_map, xq, xd, xs, xb))
+      return FQ_ERR_CUDA;
+  }
+  // Schedule: whole tiles when they fill the SMs, else stream-K over one CTA
+  // per SM, at least 4 K blocks per CTA (a CTA's fixed cost - tensor-memory
+  // set-up, pipeline fill, hand-off - grows with the number of CTAs sharing a
+  // tile).  FQ_FORCE_SCHEDULE (tests and studies): dp gives every CTA one
+  // whole tile, streamk never rounds to whole tiles, k2 halves each tile;
+  // FQ_EINSUM_BM = 64 | 128 fixes the tile rows.
   // stages in flight: about 120 KB per SM (see the W8A8 GEMM's stage cap)
   {
-    const int stage = 128 * 128 + mt * 128, ring = mt == 16 ? es::Cfg<16>::STAGES
-                                                 : (mt == 32 ? es::Cfg<32>::STAGES : es::Cfg<64>::STAGES);
-    int ah = (122880 + stage / 2) / stage;
+    int ah = (122880 + p.stage / 2) / p.stage;
     if (const char* v = std::getenv("FQ_STAGES_AHEAD")) ah = std::atoi(v);
-    p.ahead = ah < 2 ? 2 : (ah > ring ? ring : ah);
+    p.ahead = ah < 2 ? 2 : (ah > p.S ? p.S : ah);
   }
-  const int64_t by_work = (p.total + 3) / 4;
+  int64_t by_work = (p.total * p.KD + 3) / 4;
+  if (by_work > p.total) by_work = p.total;  // every CTA gets at least one chunk
   int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
-  {
+  const char* f = std::getenv("FQ_FORCE_SCHEDULE");
+  if (!f || std::strcmp(f, "streamk")) {
     const int g = whole_tile_grid(tiles, d.sm_count);
     if (g > 0 && g <= grid) grid = g;
   }
-  if (const char* f = std::getenv("FQ_FORCE_SCHEDULE")) {
+  if (f) {
     if (!std::strcmp(f, "dp") && tiles <= es::kMaxGrid) grid = int(tiles);
     // each tile split in two halves (partial sums: the workspace holds two slots per SM)
-    if (!std::strcmp(f, "k2") && 2 * tiles <= d.sm_count) grid = int(2 * tiles);
+    if (!std::strcmp(f, "k2") && 2 * tiles <= d.sm_count && p.KB / p.KD >= 2) grid = int(2 * tiles);
   }
   // partial-sum slots exist for sm_count CTAs; only whole-tile CTAs (grid == tiles) may exceed that
   if (grid > d.sm_count && grid != tiles) return FQ_ERR_SHAPE;
   const bool pdl = pdl_enabled();
   cudaError_t e;
   switch (mt) {
-    case 16: e = es::launch_es<16>(&tw_map, &tx_map, p, fmt, grid, s, pdl); break;
-    case 32: e = es::launch_es<32>(&tw_map, &tx_map, p, fmt, grid, s, pdl); break;
-    default: e = es::launch_es<64>(&tw_map, &tx_map, p, fmt, grid, s, pdl); break;
+    case 16: e = es::launch_es<16>(&tw_map, &tx_map, p, fmt, bm, grid, s, pdl); break;
+    case 32: e = es::launch_es<32>(&tw_map, &tx_map, p, fmt, bm, grid, s, pdl); break;
+    default: e = es::launch_es<64>(&tw_map, &tx_map, p, fmt, bm, grid, s, pdl); break;
   }
   return cuda_status(e);
 }

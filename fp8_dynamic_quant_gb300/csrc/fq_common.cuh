@@ -82,15 +82,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on phase `parity`; false if it did not complete within
-// `budget_ns` of wall-clock time.
-__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The polling loop of a bounded wait, out of line: inlined, the loop with its
+// timer reads cost a single-thread issue loop ~100 ns per wait on GB300 even
+// when the phase had already completed (one try_wait alone: ~35 ns).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > budget_ns) return false;
   }
   return true;
+}
+// Bounded wait on phase `parity`; false if it did not complete within
+// `budget_ns` of wall-clock time.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, budget_ns);
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return mbar_wait_ns(bar, parity, kWaitNs);
@@ -109,6 +115,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+// 3-D tiled load global -> shared (coordinates innermost first), completion
+// counted on `bar` in bytes.  x must be a multiple of 16 for 8-bit data.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
 }
 // 1-D bulk copy global -> shared (the TMA engine), completion counted on
@@ -202,6 +218,15 @@ __device__ __forceinline__ void tmem_relinquish() {
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// One lane of a converged warp (elect.sync over the full mask): the issuing
+// lane of warp-wide tensor-core loops.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b32 R;\n\telect.sync R|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -303,6 +328,15 @@ fq_status cuda_status(cudaError_t e);
 // Returns false on failure.
 bool tensor_map_u8_2d(CUtensorMap* out, const void* ptr, uint64_t cols, uint64_t rows, uint64_t pitch,
                       uint32_t box_cols, uint32_t box_rows);
+
+// Encodes a 3-D 8-bit tensor map: dims[0] the innermost extent in bytes,
+// strides[0] / strides[1] the byte strides of dimensions 1 and 2 (any order of
+// magnitude: a K-block axis of stride 128 under a row axis of stride D lets
+// one box fetch several K blocks of a row tile, landing as consecutive
+// 128-byte-swizzled K-major sub-tiles); box[i] elements per dimension.
+// Cached per thread like the 2-D maps.  Returns false on failure.
+bool tensor_map_u8_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3], const uint64_t strides[2],
+                      const uint32_t box[3]);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

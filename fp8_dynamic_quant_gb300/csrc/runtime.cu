@@ -154,6 +154,60 @@ bool tensor_map_u8_2d(CUtensorMap* out, const void* ptr, uint64_t cols, uint64_t
   return true;
 }
 
+namespace {
+struct Map3Entry {
+  const void* ptr;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  int dev;
+  bool valid;
+  CUtensorMap map;
+};
+constexpr int kMap3Cache = 128;
+thread_local Map3Entry t_maps3[kMap3Cache];
+}  // namespace
+
+bool tensor_map_u8_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3], const uint64_t strides[2],
+                      const uint32_t box[3]) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  uint64_t h = reinterpret_cast<uintptr_t>(ptr) >> 4;
+  for (int i = 0; i < 3; ++i) h = (h ^ dims[i]) * 0x9E3779B97F4A7C15ull ^ (uint64_t(box[i]) << (16 * i));
+  h ^= strides[0] * 0xC2B2AE3D27D4EB4Full ^ strides[1] ^ (uint64_t(dev) << 48);
+  h ^= h >> 29;
+  Map3Entry& e = t_maps3[h % kMap3Cache];
+  if (e.valid && e.ptr == ptr && e.dev == dev && e.dims[0] == dims[0] && e.dims[1] == dims[1] &&
+      e.dims[2] == dims[2] && e.strides[0] == strides[0] && e.strides[1] == strides[1] && e.box[0] == box[0] &&
+      e.box[1] == box[1] && e.box[2] == box[2]) {
+    *out = e.map;
+    return true;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), d, st, bx, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    e.valid = false;
+    return false;
+  }
+  e.ptr = ptr;
+  for (int i = 0; i < 3; ++i) {
+    e.dims[i] = dims[i];
+    e.box[i] = box[i];
+  }
+  e.strides[0] = strides[0];
+  e.strides[1] = strides[1];
+  e.dev = dev;
+  e.valid = true;
+  *out = e.map;
+  return true;
+}
+
 // One warp: lane 0 waits on an mbarrier that only it can complete.  The
 // wait is the library's bounded wait; when it gives up, the timeout flag is
 // recorded exactly as the pipelined kernels record it.

@@ -162,13 +162,22 @@ def test_einsum_within_tolerance_and_scale_formats_identical(T, G, D, N):
     assert ok, info
 
 
+@pytest.mark.parametrize("kd", [1, 2, 4])
+@pytest.mark.parametrize("bm", [128, 64])
 @pytest.mark.parametrize("sched", ["dp", "streamk"])
 @pytest.mark.parametrize("T,G,D,N", [(1, 8, 4096, 1024), (5, 8, 4096, 1024), (16, 8, 4096, 1024),
-                                     (40, 8, 4096, 1024), (3, 3, 640, 384), (9, 2, 384, 256)])
-def test_einsum_both_schedules(sched, T, G, D, N, monkeypatch):
-    """Whole 64-row tiles, one per CTA (dp, taken only when forced), and 128-row tiles split stream-K:
-    each within tolerance, packed and fp32 scales identical, repeat calls identical."""
+                                     (40, 8, 4096, 1024), (3, 3, 640, 384), (9, 2, 384, 256),
+                                     (2, 2, 768, 256)])
+def test_einsum_both_schedules(kd, bm, sched, T, G, D, N, monkeypatch):
+    """Whole tiles, one per CTA (dp), and tiles split over CTAs by chunks of
+    K blocks (stream-K); 128 and 64 weight rows per tile (M = 128 and M = 64
+    MMAs); 1, 2 or 4 K blocks per pipeline stage (one 3-D copy each; a count
+    that does not divide the K blocks or leaves too few stages is not taken):
+    each within tolerance, packed and fp32 scales identical, repeat calls
+    identical."""
     monkeypatch.setenv("FQ_FORCE_SCHEDULE", sched)
+    monkeypatch.setenv("FQ_EINSUM_BM", str(bm))
+    monkeypatch.setenv("FQ_EINSUM_KD", str(kd))
     x = synth.group_activations(T, G, D, 7300 + T + G)
     owq, osw, wq, sw = einsum_weights(G, N, D, 9)
     xg = bf16_to_dev(x)
