@@ -143,10 +143,11 @@ struct Problem {
 };
 
 // Wait that reads the CTA's abort flag only once the phase is found
-// incomplete: a shared-memory flag read per K block cost the single-thread
-// issue loop ~60 ns on GB300.
+// incomplete, with the polling loop out of line: inlined, the loop and its
+// timer reads, or a shared-memory flag read per wait, slowed the issue loops
+// by ~60-100 ns per wait on GB300 even when the phase had already completed.
 static __device__ __noinline__ bool wait_slow_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return !*abort_flag && mbar_wait_slow(bar, parity, kWaitNs);
+  return !*abort_flag && mbar_wait(bar, parity);
 }
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   return mbar_try_wait(bar, parity) || wait_slow_or_abort(bar, parity, abort_flag);

@@ -82,21 +82,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// The polling loop of a bounded wait, out of line: inlined, the loop with its
-// timer reads cost a single-thread issue loop ~100 ns per wait on GB300 even
-// when the phase had already completed (one try_wait alone: ~35 ns).
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+// Bounded wait on phase `parity`; false if it did not complete within
+// `budget_ns` of wall-clock time.
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > budget_ns) return false;
   }
   return true;
-}
-// Bounded wait on phase `parity`; false if it did not complete within
-// `budget_ns` of wall-clock time.
-__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, budget_ns);
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return mbar_wait_ns(bar, parity, kWaitNs);
