@@ -142,17 +142,6 @@ struct Problem {
   uint32_t* err;
 };
 
-// Wait that reads the CTA's abort flag only once the phase is found
-// incomplete, with the polling loop out of line: inlined, the loop and its
-// timer reads, or a shared-memory flag read per wait, slowed the issue loops
-// by ~60-100 ns per wait on GB300 even when the phase had already completed.
-static __device__ __noinline__ bool wait_slow_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return !*abort_flag && mbar_wait(bar, parity);
-}
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return mbar_try_wait(bar, parity) || wait_slow_or_abort(bar, parity, abort_flag);
-}
-
 // First K-block iteration of CTA c's stream-K range: the ranges split the
 // (tile, chunk) units evenly, floor(c * total / G) chunks of KD blocks each.
 __device__ __forceinline__ int range_begin(const Problem& p, int G, int c) {
@@ -302,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // stages in flight, and (q - S <= q - ahead) stage s is free
           if (q > p.ahead) lag.advance_chunk(KD, KB, n_it);
           const int gl = lag.g;
-          if (!wait_or_abort(&grp[gl % kGroupBars], uint32_t((gl / kGroupBars) & 1), &s_abort)) {
+          if (!mbar_wait_or_abort(&grp[gl % kGroupBars], uint32_t((gl / kGroupBars) & 1), &s_abort)) {
             if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
             s_abort = 1;
             break;
@@ -341,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // a group starts with this chunk and reuses the slots of the group two back
       if (cur.cnt == 0 && cur.g >= 2)
-        ok = wait_or_abort(&acc_empty[cur.g & 1], uint32_t(((cur.g >> 1) - 1) & 1), &s_abort);
-      if (ok) ok = wait_or_abort(&full[s], phase, &s_abort);
+        ok = mbar_wait_or_abort(&acc_empty[cur.g & 1], uint32_t(((cur.g >> 1) - 1) & 1), &s_abort);
+      if (ok) ok = mbar_wait_or_abort(&full[s], phase, &s_abort);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
         if (lane == 0) {
@@ -484,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_commit();
       __syncwarp();
       if (ec.cnt == 0) {  // a group starts: wait once for all of its MMAs
-        gok = wait_or_abort(&grp[ec.g % kGroupBars], uint32_t((ec.g / kGroupBars) & 1), &s_abort);
+        gok = mbar_wait_or_abort(&grp[ec.g % kGroupBars], uint32_t((ec.g / kGroupBars) & 1), &s_abort);
         gok = __all_sync(0xFFFFFFFFu, gok);
         if (!gok) {
           if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);

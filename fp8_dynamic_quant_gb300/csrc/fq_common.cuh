@@ -95,6 +95,19 @@ __device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity, uin
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return mbar_wait_ns(bar, parity, kWaitNs);
 }
+// Wait for tensor-core issue loops: one try_wait inline; the CTA's abort flag
+// and the bounded polling loop only once the phase is found incomplete, out of
+// line.  Inlined, the loop and its timer reads, or a shared-memory flag read
+// per wait, slowed an MMA issue loop by ~60-100 ns per wait on GB300 even when
+// the phase had already completed.  (Loops whose waits usually block keep the
+// inline mbar_wait: a call there costs more than it saves.)
+static __device__ __noinline__ bool mbar_wait_slow_or_abort(uint64_t* bar, uint32_t parity,
+                                                            volatile int* abort_flag) {
+  return !*abort_flag && mbar_wait(bar, parity);
+}
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow_or_abort(bar, parity, abort_flag);
+}
 
 // ------------------------------------------------------------ TMA (tensor copies)
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
