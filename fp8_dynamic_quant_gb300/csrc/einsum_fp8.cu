@@ -7,28 +7,32 @@
 //   Y[t, g, n] = bf16( sum_kb sx[t,g,kb] * sw[g,kb,n/128] * sum_{d in kb} xq[t,g,d] * W[g,d,n] )
 //
 // GB300 design (5th-generation tensor cores, operands straight from TMA):
-//  * Swap-AB tiles: 128 weight rows (n; exactly one weight-scale block) x MT
-//    tokens (16, 32 or 64; more tokens take several token tiles), one tile per
-//    (g, n-block, token tile).  Weights E4M3 [G, N, D] K-major, activations
-//    E4M3 [T, G, D]; both land by TMA in the 128-byte-swizzled K-major layout
-//    the MMA reads, so nothing is converted.
+//  * Swap-AB tiles: BM weight rows (n; 128 = one weight-scale block, or 64
+//    when whole 64-row tiles fill the SMs and 128-row ones do not) x MT
+//    tokens (16, 32 or 64; more tokens take several token tiles), one tile
+//    per (g, n-block, token tile).  Weights E4M3 [G, N, D] K-major,
+//    activations E4M3 [T, G, D]; both land by TMA in the 128-byte-swizzled
+//    K-major layout the MMA reads, so nothing is converted.
+//  * A pipeline stage holds KD (4, 2 or 1) consecutive K blocks of a tile,
+//    fetched by one 3-D TMA box for the weights and one for the activations.
 //  * warp 0 lane 0: TMA producer (weights of the first stages are issued at
 //    kernel entry, before the wait on the previous kernel);
-//  * warp 1: allocates tensor memory; lane 0 issues, per 128-wide K block,
-//    four tcgen05.mma kind::f8f6f4 (M = 128, N = MT, K = 32) into a fresh fp32
-//    accumulator slot in tensor memory, and commits once per group of four K
-//    blocks (a commit costs about a tensor-pipe drain): two groups of slots
-//    alternate;
+//  * warp 1: allocates tensor memory; the whole warp walks the stages and
+//    one elected lane issues, per 128-wide K block, four tcgen05.mma
+//    kind::f8f6f4 (M = BM, N = MT, K = 32) into a fresh fp32 accumulator
+//    slot in tensor memory, and commits once per group of four K blocks (two
+//    groups of slots alternate);
 //  * warps 2..5: one weight row per thread.  Per group they wait once, then
-//    per K block drain its slot (tcgen05.ld) and promote it into fp32
+//    per stage drain its slots (tcgen05.ld) and promote them into fp32
 //    registers: acc += blk * (sx[t] * sw) - the per-128-K block scaling.  The
-//    scales stream in a few blocks ahead by asynchronous copies.
-//  * Stream-K over the flattened (tile, K block) range, one CTA per SM: the
-//    partial tiles at a CTA's range ends go to workspace slots and the last
-//    CTA to finish a tile adds every contributor's slot in ascending CTA
-//    order, so the fp32 result does not depend on timing: the packed-scale
-//    and fp32-scale calls produce identical bits, and a token's row does not
-//    depend on the other tokens of the call.
+//    scales stream in 8-16 blocks ahead by asynchronous copies.
+//  * Whole tiles per CTA when they fill the SMs; otherwise stream-K over the
+//    flattened (tile, stage) range, one CTA per SM: the partial tiles at a
+//    CTA's range ends go to workspace slots and the last CTA to finish a tile
+//    adds every contributor's slot in ascending CTA order, so the fp32 result
+//    does not depend on timing: the packed-scale and fp32-scale calls produce
+//    identical bits, and a token's row does not depend on the other tokens of
+//    the call.
 //  * The scale format only changes how sx is decoded: packed byte
 //    ((g*P + kb/4)*Ta + t)*4 + kb%4 -> 2^(u-127), or the fp32 value.
 #include <cstdlib>
@@ -43,18 +47,18 @@ constexpr int kBK = 128;
 constexpr int kMaxGrid = 1024;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-// K blocks of scales in flight ahead of the promotion.  A 4-byte load takes
-// about 2 us while the weight stream saturates HBM, so a shallow prefetch
-// paces the promotion: 4 blocks ahead held it to ~0.5 us per block on GB300.
+// K blocks of scales in flight ahead of the promotion (a multiple of the
+// 4-block stage).  A 4-byte load takes ~2 us while the weight stream
+// saturates HBM; 4 to 16 blocks ahead measured the same on GB300.
 template <int MT>
 struct ScalePre {
   static constexpr int value = MT > 32 ? 8 : 16;  // the ring of 64-token tiles must fit beside the stages
 };
-// K blocks per tensor-core commit.  A tcgen05.commit costs about a pipeline
-// drain (~0.3 us measured on GB300 for decode-sized MMAs, against ~25 ns per
-// 128x16x32 MMA when they stream), so stage release and the accumulator
-// hand-off are signalled once per group of K blocks; a group also ends at
-// every stream-K segment end and at the end of the CTA's range.
+// K blocks per tensor-core commit.  A tcgen05.commit added ~80 ns to the
+// issuing loop on GB300, more than two decode-sized MMAs (~33 ns each), so
+// stage release and the accumulator hand-off are signalled once per group of
+// K blocks; a group also ends at every stream-K segment end and at the end of
+// the CTA's range.
 constexpr int kGroupBars = 24;  // ring of group-completion barriers (more than the stages)
 // Blocks per commit group (two groups of MT-column slots in tensor memory).
 template <int MT>
