@@ -47,13 +47,12 @@ constexpr int kBK = 128;
 constexpr int kMaxGrid = 1024;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
-// K blocks of scales in flight ahead of the promotion (a multiple of the
-// 4-block stage).  A 4-byte load takes ~2 us while the weight stream
-// saturates HBM; 4 to 16 blocks ahead measured the same on GB300.
-template <int MT>
-struct ScalePre {
-  static constexpr int value = MT > 32 ? 8 : 16;  // the ring of 64-token tiles must fit beside the stages
-};
+// Per-token promotion factors sx[t, kb] * sw[kb] come from a table in shared
+// memory filled for up to kTB K blocks of a tile at a time, the next piece
+// fetched while the current one is in use: per stage the promotion reads no
+// global memory.  (Fetching each stage's scale words by 4-byte asynchronous
+// copies in the promotion loop cost ~3 us a call at T = 1 on GB300.)
+constexpr int kTB = 32;
 // K blocks per tensor-core commit.  A tcgen05.commit added ~80 ns to the
 // issuing loop on GB300, more than two decode-sized MMAs (~33 ns each), so
 // stage release and the accumulator hand-off are signalled once per group of
@@ -123,7 +122,7 @@ struct Cfg {
 // throughput per SM is set by the number of copies more than by their bytes
 // (measured on GB300 with one CTA per SM streaming 256 MB: 8 KB boxes 3.3 TB/s,
 // 16 KB 6.0, 32-64 KB 6.2-6.4), so small tiles fetch several K blocks at once.
-constexpr int kStageBudget = 208 * 1024;  // ~200 KB of stages in flight per SM
+constexpr int kStageBudget = 200 * 1024;  // ~200 KB of stages in flight per SM (beside the factor table)
 constexpr int kMaxStages = 16;
 constexpr int kMinStages = 4;
 static_assert(kGroupBars > kMaxStages, "group barriers must outnumber the stages (no parity aliasing)");
@@ -230,9 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_flag, s_issued, s_consumed;
   __shared__ volatile int s_abort;
-  __shared__ __align__(16) float s_f[kEpiWarps][4 * MT];    // per-token scale factors of the current chunk
-  constexpr int kPre = ScalePre<MT>::value;
-  __shared__ __align__(16) uint32_t s_ring[kEpiWarps][kPre * (MT + 4)];  // scale words, kPre blocks ahead
+  __shared__ __align__(16) float s_tab[2][kTB * MT];  // promotion factors [piece buffer][block][token]
+  __shared__ float s_tsw[2][kTB];                     // weight-block scales of the piece
   __shared__ __align__(16) uint16_t s_ystage[16 * BM];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -390,54 +388,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool rowv = BM == 128 || lane < 16;
     const int nl = BM == 128 ? 32 * q + lane : 16 * q + (lane & 15);
     const uint32_t trow = tmem + (uint32_t(32 * q) << 16);
-    float* sf = s_f[warp - 2];
     float acc[MT];
 #pragma unroll
     for (int j = 0; j < MT; ++j) acc[j] = 0.0f;
     int tile = begin / KB, kb = begin - tile * KB, seg_kb0 = kb;
     ETile t = etile(p, tile);
     bool first_seg = true;
-    // Scales stream through a per-warp ring in shared memory, kPre blocks
-    // (kPre / 4 chunks) ahead, by asynchronous 4-byte copies (lane j copies
-    // token j's stored word, and j + 32's; lane 0 the weight-block scale): a
-    // block's promotion never waits on a global round trip.  Chunk slot: four
-    // block slots of MT token words, then sw.
-    constexpr int TPL = MT > 32 ? 2 : 1;
-    constexpr int kSlotW = MT + 4, kPreC = kPre / 4;
-    uint32_t* ring = s_ring[warp - 2];
-    int tile_p = tile, kb_p = kb;  // first block of the next chunk to fetch
-    auto issue = [&](int qq) {
-      const ETile tp = etile(p, tile_p);  // a chunk lies in one tile
-      uint32_t* cs = ring + (qq % kPreC) * (4 * kSlotW);
-      for (int kd = 0; kd < KD; ++kd) {
-        uint32_t* slot = cs + kd * kSlotW;
-        const int kbb = kb_p + kd;
-#pragma unroll
-        for (int i = 0; i < TPL; ++i) {
-          const int m = lane + 32 * i, tok = tp.tt * MT + m;
-          if (m < MT && tok < p.T) {
-            const void* src = FMT == FQ_SCALE_UE8M0_PACKED
-                                  ? static_cast<const void*>(static_cast<const uint32_t*>(p.sx) +
-                                                             (int64_t(tp.g) * p.P + (kbb >> 2)) * p.Ta + tok)
-                                  : static_cast<const void*>(static_cast<const float*>(p.sx) +
-                                                             (int64_t(tok) * p.G + tp.g) * KB + kbb);
-            cp_async4(slot + m, src);
-          }
+    // Promotion factors, a piece (<= kTB blocks of one tile) at a time:
+    // every epilogue thread copies a share of the piece's stored scale words
+    // and weight-block scales into a table buffer (4-byte asynchronous
+    // copies), then, after a barrier, turns its share into sx * sw in place.
+    auto fetch = [&](int buf, int tile_f, int kb_f, int len) {
+      const ETile tp = etile(p, tile_f);
+      uint32_t* tw = reinterpret_cast<uint32_t*>(s_tab[buf]);
+      for (int idx = etid; idx < len * MT; idx += kEpi) {
+        const int kbi = idx / MT, m = idx - kbi * MT, tok = tp.tt * MT + m, kbb = kb_f + kbi;
+        if (tok < p.T) {
+          const void* src = FMT == FQ_SCALE_UE8M0_PACKED
+                                ? static_cast<const void*>(static_cast<const uint32_t*>(p.sx) +
+                                                           (int64_t(tp.g) * p.P + (kbb >> 2)) * p.Ta + tok)
+                                : static_cast<const void*>(static_cast<const float*>(p.sx) +
+                                                           (int64_t(tok) * p.G + tp.g) * KB + kbb);
+          cp_async4(tw + idx, src);
         }
-        if (lane == 0) cp_async4(slot + MT, p.sw + (int64_t(tp.g) * KB + kbb) * p.NS + (tp.nb * BM) / 128);
       }
-      kb_p += KD;
-      if (kb_p == KB) {
-        kb_p = 0;
-        ++tile_p;
-      }
-    };
-    const int nq = n_it / KD;
-#pragma unroll 1
-    for (int it = 0; it < kPreC; ++it) {
-      if (it < nq) issue(it);
+      for (int idx = etid; idx < len; idx += kEpi)
+        cp_async4(&s_tsw[buf][idx], p.sw + (int64_t(tp.g) * KB + kb_f + idx) * p.NS + (tp.nb * BM) / 128);
       cp_async_commit();
-    }
+    };
+    auto convert = [&](int buf, int tile_f, int kb_f, int len) {
+      cp_async_wait<0>();  // this thread's copies of the piece (nothing was committed after them)
+      named_bar_sync(1, kEpi);
+      const ETile tp = etile(p, tile_f);
+      const uint32_t* tw = reinterpret_cast<const uint32_t*>(s_tab[buf]);
+      for (int idx = etid; idx < len * MT; idx += kEpi) {
+        const int kbi = idx / MT, m = idx - kbi * MT, tok = tp.tt * MT + m;
+        const float f = tok < p.T ? __fmul_rn(decode_sx<FMT>(tw[idx], kb_f + kbi), s_tsw[buf][kbi]) : 0.0f;
+        s_tab[buf][idx] = f;
+      }
+      named_bar_sync(1, kEpi);
+    };
+    // blocks of the piece starting at (tile, kb) with `left` blocks left in the range
+    auto piece_len = [&](int kb_f, int left) { return min(min(kTB - kb_f % kTB, KB - kb_f), left); };
+    const int nq = n_it / KD;
+    int pbuf = 0, pc_kb0 = kb;
+    if (nq > 0) fetch(0, tile, kb, piece_len(kb, n_it));
     // tensor-memory loads in flight at once: 64 registers' worth of blocks
     constexpr int LB = 64 / MT;
     GroupCursor<C::GROUP> ec;
@@ -445,37 +440,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool gok = true;
     for (int qi = 0; qi < nq; ++qi) {
       const bool seg_end = (kb + KD == KB) || (qi == nq - 1);
-      // the chunk's per-token factors sx[t] * sw (0 past T), through shared memory
-      cp_async_wait<kPreC - 1>();
-      __syncwarp();
-      {
-        const uint32_t* cs = ring + (qi % kPreC) * (4 * kSlotW);
-        float fv[4][TPL];
-#pragma unroll
-        for (int kd = 0; kd < 4; ++kd) {
-          if (kd < KD) {
-            const uint32_t* slot = cs + kd * kSlotW;
-            const float swv = __uint_as_float(slot[MT]);
-#pragma unroll
-            for (int i = 0; i < TPL; ++i) {
-              const int m = lane + 32 * i;
-              fv[kd][i] = (m < MT && t.tt * MT + m < p.T) ? __fmul_rn(decode_sx<FMT>(slot[m], kb + kd), swv) : 0.0f;
-            }
-          }
-        }
-        __syncwarp();  // the slots are read; their next copies may go out
-#pragma unroll
-        for (int kd = 0; kd < 4; ++kd) {
-          if (kd < KD) {
-#pragma unroll
-            for (int i = 0; i < TPL; ++i)
-              if (lane + 32 * i < MT) sf[kd * MT + lane + 32 * i] = fv[kd][i];
-          }
+      if (qi == 0 || kb % kTB == 0) {
+        // a piece starts: its factors are ready once converted; the next
+        // piece's scales go out now (its buffer's previous piece is done)
+        if (qi > 0) pbuf ^= 1;
+        const int left = n_it - qi * KD, len = piece_len(kb, left);
+        pc_kb0 = kb;
+        convert(pbuf, tile, kb, len);
+        if (len < left) {
+          const int kb_n = kb + len == KB ? 0 : kb + len, tile_n = kb + len == KB ? tile + 1 : tile;
+          fetch(pbuf ^ 1, tile_n, kb_n, piece_len(kb_n, left - len));
         }
       }
-      if (qi + kPreC < nq) issue(qi + kPreC);
-      cp_async_commit();
-      __syncwarp();
+      const float* sf = s_tab[pbuf] + (kb - pc_kb0) * MT;
       if (ec.cnt == 0) {  // a group starts: wait once for all of its MMAs
         gok = mbar_wait_or_abort(&grp[ec.g % kGroupBars], uint32_t((ec.g / kGroupBars) & 1), &s_abort);
         gok = __all_sync(0xFFFFFFFFu, gok);

@@ -167,12 +167,13 @@ def test_einsum_within_tolerance_and_scale_formats_identical(T, G, D, N):
 @pytest.mark.parametrize("sched", ["dp", "streamk"])
 @pytest.mark.parametrize("T,G,D,N", [(1, 8, 4096, 1024), (5, 8, 4096, 1024), (16, 8, 4096, 1024),
                                      (40, 8, 4096, 1024), (3, 3, 640, 384), (9, 2, 384, 256),
-                                     (2, 2, 768, 256)])
+                                     (2, 2, 768, 256), (3, 2, 8192, 256), (1, 1, 5120, 128)])
 def test_einsum_both_schedules(kd, bm, sched, T, G, D, N, monkeypatch):
     """Whole tiles, one per CTA (dp), and tiles split over CTAs by chunks of
     K blocks (stream-K); 128 and 64 weight rows per tile (M = 128 and M = 64
     MMAs); 1, 2 or 4 K blocks per pipeline stage (one 3-D copy each; a count
-    that does not divide the K blocks or leaves too few stages is not taken):
+    that does not divide the K blocks or leaves too few stages is not taken);
+    D = 8192 and 5120 take the promotion factors in several pieces per tile:
     each within tolerance, packed and fp32 scales identical, repeat calls
     identical."""
     monkeypatch.setenv("FQ_FORCE_SCHEDULE", sched)
