@@ -108,6 +108,10 @@ static __device__ __noinline__ bool mbar_wait_slow_or_abort(uint64_t* bar, uint3
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   return mbar_try_wait(bar, parity) || mbar_wait_slow_or_abort(bar, parity, abort_flag);
 }
+// The same order with the polling loop inline, for loops whose waits often block.
+__device__ __forceinline__ bool mbar_wait_try_first(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_try_wait(bar, parity) || (!*abort_flag && mbar_wait(bar, parity));
+}
 
 // ------------------------------------------------------------ TMA (tensor copies)
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
     int kb = begin % KB;
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
-      if (s_abort || !mbar_wait(&full[s], uint32_t((r / S) & 1))) {
+      if (!mbar_wait_try_first(&full[s], uint32_t((r / S) & 1), &s_abort)) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
         break;
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
       const uint32_t par = uint32_t((r / S) & 1);
-      bool ok = !s_abort && mbar_wait(&full[s], par) && mbar_wait(&xready[s], par);
+      bool ok = mbar_wait_try_first(&full[s], par, &s_abort) && mbar_wait_try_first(&xready[s], par, &s_abort);
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
@@ -845,7 +845,7 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
     };
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
-      bool ok = !s_abort && mbar_wait(&full[s], uint32_t((r / S) & 1));
+      bool ok = mbar_wait_try_first(&full[s], uint32_t((r / S) & 1), &s_abort);
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
@@ -1256,8 +1256,8 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       // one poll before the abort flag is read (a flag read per block measured
       // ~0.5 us over 16 blocks at M=64)
       const uint32_t pr = uint32_t((r / SR) & 1), po = uint32_t((r / SO - 1) & 1);
-      bool ok = mbar_try_wait(&raw_full[sr], pr) || (!s_abort && mbar_wait(&raw_full[sr], pr));
-      if (ok && r >= SO) ok = mbar_try_wait(&op_empty[so], po) || (!s_abort && mbar_wait(&op_empty[so], po));
+      bool ok = mbar_wait_try_first(&raw_full[sr], pr, &s_abort);
+      if (ok && r >= SO) ok = mbar_wait_try_first(&op_empty[so], po, &s_abort);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
