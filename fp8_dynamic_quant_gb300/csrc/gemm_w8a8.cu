@@ -1033,6 +1033,7 @@ __global__ void __launch_bounds__(um::kThreads, 1)
   __shared__ __align__(16) float s_sx[MT];
   __shared__ __align__(16) uint16_t s_ystage[16 * 128];  // epilogue staging: 16 tokens x 128 rows of bf16
   __shared__ int s_flag, s_issued, s_consumed;
+  __shared__ int s_conv[2];         // k-blocks each converter group finished
   __shared__ volatile int s_abort;  // set after any timed-out wait: later waits are skipped
   __shared__ int tile_start_s[GROUPED ? 1025 : 1];
   __shared__ int rb[kMaxGrid + 1];
@@ -1042,10 +1043,10 @@ __global__ void __launch_bounds__(um::kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < SR; ++i) {
       mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], um::kConvWarps);
+      mbar_init(&raw_empty[i], um::kConvWarps / 2);
     }
     for (int i = 0; i < SO; ++i) {
-      mbar_init(&op_full[i], um::kConvWarps);
+      mbar_init(&op_full[i], um::kConvWarps / 2);
       mbar_init(&op_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -1056,6 +1057,7 @@ __global__ void __launch_bounds__(um::kThreads, 1)
     fence_barrier_init();
     s_issued = 0;
     s_consumed = 0;
+    s_conv[0] = s_conv[1] = 0;
     s_abort = 0;
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
@@ -1244,15 +1246,23 @@ __global__ void __launch_bounds__(um::kThreads, 1)
     // Let the next kernel launch only once this one's inputs are final: a
     // dependent may prefetch weights before its own wait.
     pdl_launch_dependents();
-    const int cw = warp - 2, q = warp & 3, hh = cw >> 2;
+    // Two groups of four warps take alternate k-blocks (two blocks in flight:
+    // each warp's wait / load / convert / store / fence chain overlaps the
+    // other group's); warp w of a group reaches tensor-memory lanes
+    // 32*(w%4)..+31 and converts both 64-byte K halves of its rows.
+    const int cw = warp - 2, q = warp & 3, grp = cw >> 2, gw = cw & 3;
+    constexpr int kGrp = kConv / 2, XTG = 2 * XT;      // threads and activation tasks per group
     const int nl = 32 * q + lane;                       // weight row of the tile (tensor-memory lane)
     const uint32_t lane_off = uint32_t(32 * q) << 16;
     const uint32_t raw_base = smem_u32(raw), xf_base = smem_u32(xf);
-    int tile = begin / KB, kb = begin - tile * KB;
-    int consumed = 0;
-    int rows_cur = n_it > 0 ? decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s).rows : 0;
-    for (int r = 0; r < n_it; ++r) {
+    int consumed = 0, tile_cur = -1, rows_cur = 0;
+    for (int r = grp; r < n_it; r += 2) {
       const int sr = r % SR, so = r % SO;
+      const int tile = (begin + r) / KB;
+      if (tile != tile_cur) {
+        tile_cur = tile;
+        rows_cur = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s).rows;
+      }
       // one poll before the abort flag is read (a flag read per block measured
       // ~0.5 us over 16 blocks at M=64)
       const uint32_t pr = uint32_t((r / SR) & 1), po = uint32_t((r / SO - 1) & 1);
@@ -1265,25 +1275,28 @@ __global__ void __launch_bounds__(um::kThreads, 1)
         break;
       }
       const uint32_t st = raw_base + uint32_t(sr * C::RAW);
-      uint4 v[4];
+      uint4 xv[XTG];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) v[c] = lds128(st + uint32_t(nl * kBK + (((4 * hh + c) ^ (nl & 7)) << 4)));
-      uint4 xv[XT];
-#pragma unroll
-      for (int t = 0; t < XT; ++t) {
-        const int task = t * kConv + cw * 32 + lane, xr = task >> 3, xc = task & 7;
+      for (int t = 0; t < XTG; ++t) {
+        const int task = t * kGrp + gw * 32 + lane, xr = task >> 3, xc = task & 7;
         if (xr < rows_cur) xv[t] = lds128(st + uint32_t(C::W_BYTES + xr * kBK + ((xc ^ (xr & 7)) << 4)));
       }
-      uint32_t a[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int hh = 0; hh < 2; ++hh) {
+        uint4 v[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) i8x4_to_f16(word_of(v[c], i), a[8 * c + 2 * i], a[8 * c + 2 * i + 1]);
-      tmem_st32(tmem + lane_off + uint32_t(C::ACC_COLS + so * 64 + 32 * hh), a);
+        for (int c = 0; c < 4; ++c) v[c] = lds128(st + uint32_t(nl * kBK + (((4 * hh + c) ^ (nl & 7)) << 4)));
+        uint32_t a[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) i8x4_to_f16(word_of(v[c], i), a[8 * c + 2 * i], a[8 * c + 2 * i + 1]);
+        tmem_st32(tmem + lane_off + uint32_t(C::ACC_COLS + so * 64 + 32 * hh), a);
+      }
       const uint32_t xs = xf_base + uint32_t(so * C::XF);
 #pragma unroll
-      for (int t = 0; t < XT; ++t) {
-        const int task = t * kConv + cw * 32 + lane, xr = task >> 3, xc = task & 7;
+      for (int t = 0; t < XTG; ++t) {
+        const int task = t * kGrp + gw * 32 + lane, xr = task >> 3, xc = task & 7;
         if (xr < rows_cur) {
           uint32_t f[8];
 #pragma unroll
@@ -1306,13 +1319,8 @@ __global__ void __launch_bounds__(um::kThreads, 1)
         mbar_arrive(&op_full[so]);
       }
       ++consumed;
-      if (++kb == KB) {
-        kb = 0;
-        ++tile;
-        if (r + 1 < n_it) rows_cur = decode_tile<MT, 128, GROUPED>(p, tile, tile_start_s).rows;
-      }
     }
-    if (tid == 64) s_consumed = consumed;
+    if (gw == 0 && lane == 0) s_conv[grp] = consumed;
   } else {
     // ------------------------------------------------ epilogue
     pdl_wait();
@@ -1475,7 +1483,9 @@ __global__ void __launch_bounds__(um::kThreads, 1)
   // Drain: on the normal path every issued stage was consumed.  After a
   // timeout, wait (bounded) for copies still in flight before exiting.
   if (tid == 0) {
-    for (int r = s_consumed; r < s_issued; ++r) mbar_wait(&raw_full[r % SR], uint32_t((r / SR) & 1));
+    // blocks 0 .. 2*c0-2 went to group 0, 1 .. 2*c1-1 to group 1: the contiguous prefix converted
+    const int done = min(2 * s_conv[0], 2 * s_conv[1] + 1);
+    for (int r = done; r < s_issued; ++r) mbar_wait(&raw_full[r % SR], uint32_t((r / SR) & 1));
   }
   if (warp == 1) {
     tc_fence_after();
