@@ -951,14 +951,15 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
 // operand in tensor memory and fp32 accumulators in tensor memory:
 //  - warp 0, lane 0: TMA producer of raw int8 stages (128 weight rows x 128 K
 //    and MT tokens x 128 K), the same stream-K walk as the kernel above;
-//  - warps 2..9: converters.  Warp w reaches tensor-memory lanes
-//    32*(w%4)..32*(w%4)+31 and takes K half (w-2)/4 of each k-block: every
-//    thread turns 64 bytes of its weight row into f16 pairs and stores them
-//    to the k-block's A stage with tcgen05.st.  Together they convert the
+//  - warps 2..9: converters, two groups of four taking alternate k-blocks.
+//    Warp w reaches tensor-memory lanes 32*(w%4)..32*(w%4)+31: every thread
+//    turns the 128 bytes of its weight row into f16 pairs and stores them to
+//    the k-block's A stage with tcgen05.st.  Together a group converts the
 //    activation tile into a 128-byte-swizzled K-major f16 operand in shared
 //    memory.
-//  - warp 1: allocates tensor memory; lane 0 issues tcgen05.mma kind::f16
-//    (M = 128 weight rows, N = MT tokens, K = 16) and commits each stage back.
+//  - warp 1: allocates tensor memory; the whole warp walks the k-blocks and
+//    an elected lane issues tcgen05.mma kind::f16 (M = 128 weight rows,
+//    N = MT tokens, K = 16) and commits each stage back.
 //  - warps 10..13: epilogue, one weight row per thread.  They drain each
 //    finished accumulator region into exact int32 sums kept in tensor memory
 //    and, at a segment's end, run the stream-K hand-off and the dequantizing
