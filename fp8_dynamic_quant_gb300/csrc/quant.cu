@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(MAXT) dynamic_quant_int8_kernel(const uint4* _
 // with the next row's loads issued before the current row is reduced and
 // stored, so each CTA keeps two rows of loads in flight; the block reduction
 // scratch alternates between two buffers, which saves its trailing barrier.
-template <int VPT, int MAXT, int MINB>
+template <int VPT, int MAXT, int MINB, int AH = 1>
 __global__ void __launch_bounds__(MAXT, MINB) quant_int8_stream_kernel(const uint4* __restrict__ x, int64_t M, int64_t K8,
                                                                  uint2* __restrict__ q, float* __restrict__ s,
                                                                  int trigger) {
@@ -110,26 +110,29 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_int8_stream_kernel(const uin
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
   int64_t row = blockIdx.x;
   if (row >= M) return;
-  uint4 cur[VPT], nxt[VPT];
+  // rows row, row + grid, ..., row + AH * grid in flight (pre[0] = the current row;
+  // 2 or 3 rows ahead measured no faster than 1 at M=16384, K=4096 on GB300)
+  uint4 pre[AH + 1][VPT];
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int64_t idx = tid + int64_t(i) * nt;
-    cur[i] = idx < K8 ? ld_stream(x + row * K8 + idx) : make_uint4(0, 0, 0, 0);
-  }
-  for (int par = 0; row < M; row += gridDim.x, par ^= 1) {
-    const int64_t next = row + gridDim.x;
+  for (int a = 0; a < AH; ++a) {
+    const int64_t rr = row + int64_t(a) * gridDim.x;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int64_t idx = tid + int64_t(i) * nt;
-      nxt[i] = (next < M && idx < K8) ? ld_stream(x + next * K8 + idx) : make_uint4(0, 0, 0, 0);
+      pre[a][i] = (rr < M && idx < K8) ? ld_stream(x + rr * K8 + idx) : make_uint4(0, 0, 0, 0);
+    }
+  }
+  uint4 (&cur)[VPT] = pre[0];
+  for (int par = 0; row < M; row += gridDim.x, par ^= 1) {
+    const int64_t next = row + int64_t(AH) * gridDim.x;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int64_t idx = tid + int64_t(i) * nt;
+      pre[AH][i] = (next < M && idx < K8) ? ld_stream(x + next * K8 + idx) : make_uint4(0, 0, 0, 0);
     }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      float f[8];
-      unpack8(cur[i], f);
-      amax = fmaxf(amax, absmax8(f));
-    }
+    for (int i = 0; i < VPT; ++i) amax = fmaxf(amax, absmax8_bf16(cur[i]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     if (lane == 0) red[par][warp] = amax;
@@ -149,7 +152,8 @@ __global__ void __launch_bounds__(MAXT, MINB) quant_int8_stream_kernel(const uin
         unpack8(cur[i], f);
         qr[idx] = quant8_i8(f, sc, inv);
       }
-      cur[i] = nxt[i];
+#pragma unroll
+      for (int a = 0; a < AH; ++a) pre[a][i] = pre[a + 1][i];
     }
   }
 }
@@ -875,7 +879,9 @@ using namespace fq;
 //    critical path is the per-thread quant arithmetic and the block barrier.
 //  * many rows: CTAs of 256 threads, grid-stride over rows, the next row's
 //    loads in flight while the current one is reduced and stored ("row"):
-//    60 us at M = 16384 (0.49 of HBM).
+//    50 us at M = 16384 (0.59 of HBM; 60 us before the packed-pair absmax
+//    and the eight-at-a-time code path - the kernel is issue-bound, ~22
+//    instructions an element, a third of them per-row reduction and scale).
 //  * built, tested, taken only when forced: 256-thread rows without the
 //    prefetch (2.35-2.8 / 1.82-2.2; 66.5 us), rows staged through a
 //    shared-memory ring by bulk copies 8-16 rows ahead ("ring", 70 us), one
