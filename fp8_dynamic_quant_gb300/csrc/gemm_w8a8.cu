@@ -451,9 +451,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
           const int idx = lane + 32 * i;
           if (idx < K8) {
             v[i] = ld_stream(xr + idx);
-            float f[8];
-            unpack8(v[i], f);
-            amax = fmaxf(amax, absmax8(f));
+            amax = fmaxf(amax, absmax8_bf16(v[i]));
           }
         }
 #pragma unroll

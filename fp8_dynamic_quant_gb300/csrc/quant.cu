@@ -64,16 +64,10 @@ __global__ void __launch_bounds__(MAXT) dynamic_quant_int8_kernel(const uint4* _
       const int64_t idx = tid + int64_t(i) * nt;
       if (idx < K8) {
         v[i] = ld_stream(xr + idx);
-        float f[8];
-        unpack8(v[i], f);
-        amax = fmaxf(amax, absmax8(f));
+        amax = fmaxf(amax, absmax8_bf16(v[i]));
       }
     }
-    for (int64_t idx = tid + int64_t(VPT) * nt; idx < K8; idx += nt) {
-      float f[8];
-      unpack8(xr[idx], f);
-      amax = fmaxf(amax, absmax8(f));
-    }
+    for (int64_t idx = tid + int64_t(VPT) * nt; idx < K8; idx += nt) amax = fmaxf(amax, absmax8_bf16(xr[idx]));
     amax = block_max(amax, red);
     const float sc = __fdiv_rn(amax, 127.0f);
     const float inv = __frcp_rn(sc);
@@ -202,9 +196,7 @@ __global__ void __launch_bounds__(256, 3) quant_int8_ring_kernel(const uint4* __
     for (int j = 0; j < VPT; ++j) {
       const int64_t idx = tid + 256 * j;
       v[j] = (ok && idx < K8) ? src[idx] : make_uint4(0, 0, 0, 0);
-      float f[8];
-      unpack8(v[j], f);
-      amax = fmaxf(amax, absmax8(f));
+      amax = fmaxf(amax, absmax8_bf16(v[j]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -263,11 +255,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) quant_int8_warp_kernel(const ui
     }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      float f[8];
-      unpack8(v[i], f);
-      amax = fmaxf(amax, absmax8(f));
-    }
+    for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, absmax8_bf16(v[i]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     const float sc = __fdiv_rn(amax, 127.0f);
