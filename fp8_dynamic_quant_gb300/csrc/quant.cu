@@ -865,11 +865,12 @@ using namespace fq;
 //    16-byte vector a thread for K <= 8192 ("wide"): 1.96-2.15 / 1.79-2.06.
 //    A decode-sized row is one round trip to memory; what remains on the
 //    critical path is the per-thread quant arithmetic and the block barrier.
-//  * many rows: CTAs of 256 threads, grid-stride over rows, the next row's
-//    loads in flight while the current one is reduced and stored ("row"):
-//    50 us at M = 16384 (0.59 of HBM; 60 us before the packed-pair absmax
-//    and the eight-at-a-time code path - the kernel is issue-bound, ~22
-//    instructions an element, a third of them per-row reduction and scale).
+//  * many rows: CTAs of 256 threads (128 for 2048 < K <= 4096), grid-stride
+//    over rows, the next row's loads in flight while the current one is
+//    reduced and stored ("row"): 44 us at M = 16384 (0.67 of HBM; 60 us
+//    before the packed-pair absmax, the eight-at-a-time code path and the
+//    128-thread rows - the kernel is issue-bound, ~21 instructions an element
+//    at 256 threads, a third of them per-row reduction and scale).
 //  * built, tested, taken only when forced: 256-thread rows without the
 //    prefetch (2.35-2.8 / 1.82-2.2; 66.5 us), rows staged through a
 //    shared-memory ring by bulk copies 8-16 rows ahead ("ring", 70 us), one
@@ -964,6 +965,14 @@ fq_status fq::quant_int8_launch(const uint16_t* x, int64_t M, int64_t K, int8_t*
     const int threads = force == QK_ROW ? (K8 >= 256 ? 256 : int(t32)) : int(t32 < 1024 ? t32 : 1024);
     const int64_t vpt = (K8 + threads - 1) / threads;
     if (force == QK_ROW) {
+      if (K8 > 256 && K8 <= 512) {
+        // 128 threads, four vectors each: the per-row reduction and scale
+        // spread over twice the elements (the kernel is issue-bound: 50 -> 44 us
+        // at M=16384, K=4096 on GB300)
+        const int grid = grid_for(M, 1, d.sm_count, 8);
+        e = launch(quant_int8_stream_kernel<4, 128, 8>, grid, 128, 0, s, pdl, xp, M, K8, qp, sx, tr);
+        return cuda_status(e);
+      }
       const int grid = grid_for(M, 1, d.sm_count, 6 * 256 / threads);
       if (vpt <= 1)
         e = launch(quant_int8_stream_kernel<1, 256, 6>, grid, threads, 0, s, pdl, xp, M, K8, qp, sx, tr);

@@ -25,7 +25,8 @@ def gpu_quant(x_bits):
 @pytest.mark.parametrize("M,K", [(1, 4096), (2, 4096), (3, 4096), (4, 4096), (7, 1024), (8, 1024), (9, 4096),
                                  (16, 1024), (32, 4096), (64, 4096), (129, 1024), (5, 16), (3, 4112),
                                  (2, 16400), (300, 64), (1, 2048 * 8 * 4 + 16),
-                                 (1216, 4096), (1300, 1024), (2000, 16), (1500, 528)])  # warp-per-row path
+                                 (1216, 4096), (1300, 1024), (2000, 16), (1500, 528),   # warp-per-row path
+                                 (1300, 3072), (400, 2064)])  # 128-thread rows, ragged vectors a thread
 def test_dynamic_quant_bit_exact(M, K):
     x = synth.activations(M, K, 1000 + M * 7 + K)
     q, s = gpu_quant(x)
