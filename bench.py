@@ -891,8 +891,11 @@ def run_profile_case(name):
     each call on its own weight copy; fused_K1024_N32768: the fused quant + GEMM
     the same way; einsum_T<T>: the block-scaled FP8 einsum
     (G=8, D=4096, N=1024) three times; int8_quant_M16384: the per-token quant
-    at M=16384, K=4096 twice; fp8_group_quant_T4096: the group quant with packed
-    UE8M0 scales at T=4096, G=8, D=4096 twice.  Prints one status line."""
+    at M=16384, K=4096 twice; rmsnorm_quant_M16384: RMSNorm + INT8 quant at
+    M=16384, K=4096 twice; mxfp8_K4096_N1024 / mxfp8_K1024_N32768: the
+    32-element block-scaled linear at M=16 three times on one weight set;
+    fp8_group_quant_T4096: the group quant with packed UE8M0 scales at T=4096,
+    G=8, D=4096 twice.  Prints one status line."""
     import torch
     import fp8_dynamic_quant_gb300 as fq
     from fp8_dynamic_quant_gb300 import synth
@@ -936,6 +939,23 @@ def run_profile_case(name):
         x = bf(synth.activations(16384, 4096, SEED + 9))
         for _ in range(2):
             fq.dynamic_quant_int8(x)
+            launches += 1
+    elif name == "rmsnorm_quant_M16384":
+        x = bf(synth.activations(16384, 4096, SEED + 61))
+        gam = bf(synth.activations(1, 4096, SEED + 60)[0])
+        for _ in range(2):
+            fq.rmsnorm_quant_int8(x, gam, 1e-6)
+            launches += 1
+    elif name.startswith("mxfp8_"):
+        K, N = {"mxfp8_K4096_N1024": (4096, 1024), "mxfp8_K1024_N32768": (1024, 32768)}[name]
+        wb = (torch.randn((N, K), generator=torch.Generator(device=dev).manual_seed(SEED + 80), device=dev) * 0.02).to(
+            torch.bfloat16)
+        wq, wsf = fq.quant_mxfp8(wb)
+        del wb
+        qx, sxb = fq.quant_mxfp8(bf(synth.activations(16, K, SEED + 81 + 16)))
+        ws = fq.new_workspace(fq.workspace_bytes(fq.OP_MXFP8_LINEAR, 16, K, N), dev)
+        for _ in range(3):
+            fq.mxfp8_linear(qx, sxb, wq, wsf, ws=ws)
             launches += 1
     elif name == "fp8_group_quant_T4096":
         x = bf(synth.group_activations(4096, 8, 4096, SEED + 2))
