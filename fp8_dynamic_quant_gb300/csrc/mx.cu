@@ -457,7 +457,12 @@ extern "C" __attribute__((visibility("default"))) fq_status mxfp8_linear(const u
     if (const char* v = std::getenv("FQ_STAGES_AHEAD")) ah = std::atoi(v);
     p.ahead = ah < 2 ? 2 : ah;
   }
-  const int64_t by_work = (p.total + 3) / 4;
+  // at least 4 k-blocks a CTA, 8 with 64- or 128-token tiles: a tile's last
+  // CTA adds its partners' partial slots (128 x MT fp32 each) on the critical
+  // path, so fewer partners pay off once the slots are large (K=4096, N=1024
+  // on GB300: M=64 13.7 -> 11.0 us, M=128 23.1 -> 15.9 us)
+  const int minb = mt >= 64 ? 8 : 4;
+  const int64_t by_work = (p.total + minb - 1) / minb;
   int grid = int(by_work < d.sm_count ? (by_work > 0 ? by_work : 1) : d.sm_count);
   {
     const int g = whole_tile_grid(tiles, d.sm_count);

@@ -100,6 +100,29 @@ def test_dynamic_quant_near_half_integers():
     assert np.array_equal(s.view(np.uint32), os_.view(np.uint32)) and np.array_equal(q, oq)
 
 
+@pytest.mark.parametrize("K", [4096, 2064, 1024])
+def test_dynamic_quant_edge_rows_many_rows(K):
+    """The many-rows kernels (M above the SM count; 128-thread rows for 2048 < K <= 4096) on zero rows,
+    bf16 subnormals, values near the bf16 maximum and quotients at k + 0.5, between ordinary rows."""
+    r = np.random.default_rng(17 + K)
+    M = 320
+    x = r.standard_normal((M, K)).astype(np.float32)
+    x[5] = 0.0                                                       # all-zero row: s = 0, q = 0
+    x[6] = 0.0
+    x[6, :3] = [1e-39, -3e-39, 2e-40]                                # subnormal-only row
+    x[7] = r.uniform(-3.0e38, 3.0e38, K).astype(np.float32)         # near the bf16 maximum
+    amax = 127.0 * 1.5
+    k = r.integers(-126, 126, K).astype(np.float64) + 0.5
+    x[8] = (k * (amax / 127.0)).astype(np.float32)                   # quotients at half-integers
+    x[8, 0] = amax
+    x[M - 1] = -x[M - 1]
+    xb = codecs.f32_to_bf16(x)
+    q, s = gpu_quant(xb)
+    oq, os_ = oi8.dynamic_quant_int8(xb)
+    assert np.array_equal(s.view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(q, oq)
+
+
 def gpu_linear(q, s, w, sw):
     y = fq.w8a8_linear(np_to_dev(q), np_to_dev(s), np_to_dev(w), np_to_dev(sw))
     torch.cuda.synchronize()
