@@ -973,17 +973,19 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = (2 + kConvWarps + kEpiWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 
-// Tensor-memory columns: [2 buffers][CH chains] fp32 accumulator regions of
-// MT columns, then OP_STAGES A stages of 64 columns, then MT columns of
-// int32 segment sums.  At N = MT <= 64 one MMA is short next to its latency,
-// so the K steps of a chunk go round-robin to CH independent accumulators
-// that the tensor pipe can overlap.
+// Tensor-memory columns: [2 buffers] fp32 accumulator regions of MT columns
+// (one chain: the K steps of a chunk accumulate into one region - measured as
+// fast as four independent chains), then OP_STAGES A stages of 64 columns,
+// then MT columns of int32 segment sums.  The A stages pace the pipeline
+// (converters -> MMA -> stage released): 5 at 64 tokens and 6 at 32, against
+// 3 and 4 with the four-chain layout, took K=1024, N=32768, M=64 from 12.6 to
+// 12.2 us and M=32 from 11.6 to 10.8 us on GB300.
 template <int MT>
 struct Cfg {
-  static constexpr int CH = MT == 32 ? 4 : 2;
+  static constexpr int CH = 1;
   static constexpr int ACC_COLS = 2 * CH * MT;
   static constexpr int OP_FIT = (int(kTmemCols) - ACC_COLS - MT) / 64;
-  static constexpr int OP_STAGES = OP_FIT > 4 ? 4 : OP_FIT;
+  static constexpr int OP_STAGES = OP_FIT > 6 ? 6 : OP_FIT;
   static constexpr int ISUM_COL = ACC_COLS + OP_STAGES * 64;
   static constexpr int W_BYTES = 128 * kBK;       // raw weights of a stage
   static constexpr int X_BYTES = MT * kBK;        // raw activations of a stage
@@ -1625,10 +1627,11 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
   const int KB = int((K + kBK - 1) / kBK);
   // Schedule.  When tiles of 224 weight rows (14 consumer warps) give between
   // 3/4 of and one tile per SM, every CTA streams one whole tile: no split-K,
-  // no partial sums.  Otherwise 128-row tiles are split stream-K over one CTA
-  // per SM.  (224-row tiles need MT <= 32 to fit the register file.)
+  // no partial sums - for token tiles up to 16; at 32 the tcgen05 kernel is
+  // ahead (K=1024, N=32768 on GB300: 10.8 against 11.4 us).  Otherwise
+  // 128-row tiles are split stream-K over one CTA per SM.
   const int64_t tiles224 = ((N + 223) / 224) * m_tiles;
-  bool data_parallel = mt <= 32 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
+  bool data_parallel = mt <= 16 && tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
   // Few tiles (small N): 32-row tiles, each split over K by a cluster of 4 CTAs
   // with a distributed-shared-memory reduction, when that fills >= 1/2 the GPU
   // (every token tile: with its k-split warps it beats the tcgen05 kernel at 64).
