@@ -76,7 +76,10 @@ struct Cfg {
   static constexpr int STAGE = W_BYTES + (FQ ? 0 : X_BYTES);  // multiple of 1024
   static constexpr int XF = MT * kBK * 2;                     // f16 activation fragments of a stage
   static constexpr int XQ = FQ ? MT * kFuseKMax : 0;          // quantized activation tile, all of K
-  static constexpr int EPI = BN * MT * 2;                     // bf16 staging
+  // Token tiles of up to 16 store the output straight from the MMA fragments;
+  // larger ones stage it in shared memory for 16-byte stores.
+  static constexpr bool DIRECT_EPI = MT <= 16;
+  static constexpr int EPI = DIRECT_EPI ? 0 : BN * MT * 2;    // bf16 staging
   // Loaded HBM latency is several microseconds, so each SM needs ~200 KB of
   // weights in flight to stream at full rate: fill shared memory up to the
   // opt-in maximum (232448 bytes) less the kernel's static tables.
@@ -111,6 +114,7 @@ struct Problem {
   int E;                    // grouped: experts
   int w_reuse;              // weight tiles are read by more than one token tile
   int ahead;                // stages the producer keeps in flight (0: the whole ring)
+  int per_cta;              // dense: iterations per CTA when the split is uniform (host-computed), else 0
   const uint16_t* x16;      // CTA-quantized activations: bf16 [M, K]
   int8_t* xq_out;           // ... optional copy of the quantized activations [M, K]
   float* sx_out;            // ... optional copy of their scales [M]
@@ -179,7 +183,8 @@ template <int MT, int BN, bool GROUPED>
 __device__ __forceinline__ TileCoord decode_tile(const Problem& p, int tile, const int* tile_start) {
   TileCoord tc;
   if (!GROUPED) {
-    const int nt = tile / p.m_tiles, mt = tile - nt * p.m_tiles;
+    const int mtl = p.m_tiles;
+    const int nt = mtl == 1 ? tile : tile / mtl, mt = tile - nt * mtl;
     tc.w_row = nt * BN;
     tc.n0 = nt * BN;
     tc.x_row = mt * MT;
@@ -219,6 +224,13 @@ __device__ __forceinline__ int cta_of(const int* rb, int G, int i) {
   return lo;
 }
 
+// First iteration of CTA c's range in a dense problem, floor(c * total / G):
+// the host passes the per-CTA count when the split is uniform, which keeps the
+// 64-bit division off the path to a CTA's first weight copy.
+__device__ __forceinline__ int range_begin(const Problem& p, int c, int G) {
+  return p.per_cta ? c * p.per_cta : int(int64_t(c) * p.total / G);
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int MT, int CW, bool GROUPED, bool FQ = false>
 __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
@@ -253,20 +265,13 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
   // at decode sizes every cycle before the first copy adds to the kernel time.
   int pre = 0;  // weight stages already issued (producer thread)
   if (producer) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kCW);
-      mbar_init(&xready[i], 1);
-    }
+    // the barriers the first copies complete on come first; the rest after
+    for (int i = 0; i < S; ++i) mbar_init(&full[i], 1);
     fence_barrier_init();
-    s_issued = 0;
-    s_consumed = 0;
-    s_abort = 0;
     tma_prefetch_desc(&tmW);
-    tma_prefetch_desc(&tmX);
     if (!GROUPED) {
       // this CTA's stream-K range, as rb[] below tabulates it
-      const int b0 = int(int64_t(b) * p.total / G), b1 = int(int64_t(b + 1) * p.total / G);
+      const int b0 = range_begin(p, b, G), b1 = range_begin(p, b + 1, G);
       pre = min(b1 - b0, p.ahead > 0 && p.ahead < S ? p.ahead : S);
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       int tile = b0 / p.KB, kb = b0 - tile * p.KB;
@@ -280,6 +285,15 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
         }
       }
     }
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&empty[i], kCW);
+      mbar_init(&xready[i], 1);
+    }
+    fence_barrier_init();
+    s_issued = 0;
+    s_consumed = 0;
+    s_abort = 0;
+    tma_prefetch_desc(&tmX);
   }
 
   int64_t I = p.total;
@@ -321,7 +335,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
   }
   __syncthreads();
 
-  for (int c = tid; c <= G; c += kThreads) rb[c] = int(int64_t(c) * I / G);
+  for (int c = tid; c <= G; c += kThreads) rb[c] = GROUPED ? int(int64_t(c) * I / G) : range_begin(p, c, G);
   __syncthreads();
   const int begin = rb[b], end = rb[b + 1];
   const int KB = p.KB;
@@ -634,7 +648,27 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
             }
           }
         }
-        if (do_epi) {
+        if (do_epi && C::DIRECT_EPI) {
+          // Dequant and store straight from the fragments: channels rg and
+          // rg ^ 1 of a 16-row block sit in lanes l and l ^ 8 (g ^ 2), so the
+          // lane holding the even channel stores the pair as one bf16x2 word
+          // (N is a multiple of 16: the odd channel is in range with the even).
+          const bool lead = (g & 2) == 0;
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              const int nl = 16 * warp + rg + ((rr & 2) ? 8 : 0);
+              const int ml = 8 * j + frag_row(2 * c + (rr & 1));
+              const int n = tc.n0 + nl;
+              const bool in = ml < tc.rows && n < p.N;
+              float v = 0.f;
+              if (in) v = __fmul_rn(__fmul_rn(__int2float_rn(acci[j][rr]), sxr[j][rr & 1]), swr[rr >> 1]);
+              const uint32_t mine = f32_to_bf16_bits(v);
+              const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 8);
+              if (lead && in) *reinterpret_cast<uint32_t*>(p.y + int64_t(tc.x_row + ml) * p.N + n) = mine | (other << 16);
+            }
+        } else if (do_epi) {
           // dequant into the bf16 staging tile epi[m][n], then coalesced stores
 #pragma unroll
           for (int j = 0; j < NT; ++j)
@@ -1042,10 +1076,31 @@ __global__ void __launch_bounds__(um::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int i = 0; i < SR; ++i) {
-      mbar_init(&raw_full[i], 1);
-      mbar_init(&raw_empty[i], um::kConvWarps / 2);
+    // the barriers the first copies complete on come first; the rest after
+    for (int i = 0; i < SR; ++i) mbar_init(&raw_full[i], 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    // Thread 0 is the producer.  Dense problems issue their first weight
+    // stages right here: they depend on nothing, and at decode sizes every
+    // cycle before the first copy adds to the kernel time.
+    if (!GROUPED) {
+      // this CTA's stream-K range, as rb[] below tabulates it
+      const int b0 = range_begin(p, blockIdx.x, gridDim.x);
+      const int b1 = range_begin(p, blockIdx.x + 1, gridDim.x);
+      const int pre = min(b1 - b0, SR);
+      const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
+      int tile = b0 / p.KB, kb = b0 - tile * p.KB;
+      TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, nullptr);
+      for (int r = 0; r < pre; ++r) {
+        mbar_arrive_expect_tx(&raw_full[r], uint32_t(C::W_BYTES + um::x_box_rows<MT>(tc.rows) * kBK));
+        tma_load_2d(raw + r * C::RAW, &tmW, &raw_full[r], kb * kBK, tc.w_row, pol_w);
+        if (++kb == p.KB && r + 1 < pre) {
+          kb = 0;
+          tc = decode_tile<MT, 128, GROUPED>(p, ++tile, nullptr);
+        }
+      }
     }
+    for (int i = 0; i < SR; ++i) mbar_init(&raw_empty[i], um::kConvWarps / 2);
     for (int i = 0; i < SO; ++i) {
       mbar_init(&op_full[i], um::kConvWarps / 2);
       mbar_init(&op_empty[i], 1);
@@ -1060,30 +1115,9 @@ __global__ void __launch_bounds__(um::kThreads, 1)
     s_consumed = 0;
     s_conv[0] = s_conv[1] = 0;
     s_abort = 0;
-    tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmX16);
     tma_prefetch_desc(&tmX32);
-    // Thread 0 is the producer.  Dense problems issue their first weight
-    // stages right here: they depend on nothing, and at decode sizes every
-    // cycle before the first copy adds to the kernel time.
-    if (!GROUPED) {
-      // this CTA's stream-K range, as rb[] below tabulates it
-      const int b0 = int(int64_t(blockIdx.x) * p.total / gridDim.x);
-      const int b1 = int(int64_t(blockIdx.x + 1) * p.total / gridDim.x);
-      const int pre = min(b1 - b0, SR);
-      const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
-      int tile = b0 / p.KB, kb = b0 - tile * p.KB;
-      TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, nullptr);
-      for (int r = 0; r < pre; ++r) {
-        mbar_arrive_expect_tx(&raw_full[r], uint32_t(C::W_BYTES + um::x_box_rows<MT>(tc.rows) * kBK));
-        tma_load_2d(raw + r * C::RAW, &tmW, &raw_full[r], kb * kBK, tc.w_row, pol_w);
-        if (++kb == p.KB && r + 1 < pre) {
-          kb = 0;
-          tc = decode_tile<MT, 128, GROUPED>(p, ++tile, nullptr);
-        }
-      }
-    }
   }
   if (warp == 1) {
     tmem_alloc(&s_tmem, um::kTmemCols);
@@ -1127,7 +1161,7 @@ __global__ void __launch_bounds__(um::kThreads, 1)
     I = int64_t(tile_start_s[p.E]) * p.KB;
   }
   const int G = gridDim.x, b = blockIdx.x;
-  for (int c = tid; c <= G; c += kThreads) rb[c] = int(int64_t(c) * I / G);
+  for (int c = tid; c <= G; c += kThreads) rb[c] = GROUPED ? int(int64_t(c) * I / G) : range_begin(p, c, G);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1721,6 +1755,7 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     const int g = whole_tile_grid(tiles, d.sm_count);
     if (g > 0 && g <= grid) grid = g;
   }
+  p.per_cta = p.total % grid == 0 ? int(p.total / grid) : 0;
   debug_schedule("w8a8_linear", M, K, N, mt_run, data_parallel ? "dp224" : (umma ? "umma" : "streamk"), grid);
   const bool pdl = pdl_enabled();
   cudaError_t e;
@@ -1811,6 +1846,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
     p.m_tiles = 1;
     p.n_tiles = int(tiles);
     p.total = tiles * p.KB;
+    p.per_cta = p.KB;  // one whole tile per CTA
     p.sw = sw;
     p.y = y;
     p.counters = reinterpret_cast<uint32_t*>(w8);
