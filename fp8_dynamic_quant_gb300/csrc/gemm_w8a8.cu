@@ -46,6 +46,7 @@
 //    the next kernel start only once they have finished.)
 #include <cuda_fp16.h>
 
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -99,11 +100,18 @@ struct Cfg {
 // touches all 32 banks once.
 __device__ __forceinline__ int frag_row(int g) { return (g >> 1) | ((g & 1) << 2); }
 
+// The fields a producer reads before its first weight copies come first, so
+// that they share one constant-cache line: each extra line is a miss on the
+// path to the first copy.
 struct Problem {
   int M, N, K, KB;          // tokens (dense) / rows (grouped), channels, depth, k-blocks
   int m_tiles;              // dense: tiles along M
   int n_tiles;              // tiles along N
   int64_t total;            // dense: total iterations (tiles * KB); grouped: computed on device
+  int per_cta;              // dense: iterations per CTA when the split is uniform (host-computed), else 0
+  int ahead;                // stages the producer keeps in flight (0: the whole ring)
+  int w_reuse;              // weight tiles are read by more than one token tile
+  int E;                    // grouped: experts
   const float* sx;          // [M] or [R]
   const float* sw;          // [N] or [E, N]
   uint16_t* y;              // [M, N] or [R, N]
@@ -111,14 +119,11 @@ struct Problem {
   uint32_t* counters;       // per tile
   uint32_t* err;
   const int32_t* offsets;   // grouped: [E + 1]
-  int E;                    // grouped: experts
-  int w_reuse;              // weight tiles are read by more than one token tile
-  int ahead;                // stages the producer keeps in flight (0: the whole ring)
-  int per_cta;              // dense: iterations per CTA when the split is uniform (host-computed), else 0
   const uint16_t* x16;      // CTA-quantized activations: bf16 [M, K]
   int8_t* xq_out;           // ... optional copy of the quantized activations [M, K]
   float* sx_out;            // ... optional copy of their scales [M]
 };
+static_assert(offsetof(Problem, sx) == 48, "producer set-up fields within the first 64 bytes");
 
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -274,7 +279,8 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
       const int b0 = range_begin(p, b, G), b1 = range_begin(p, b + 1, G);
       pre = min(b1 - b0, p.ahead > 0 && p.ahead < S ? p.ahead : S);
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
-      int tile = b0 / p.KB, kb = b0 - tile * p.KB;
+      // one whole tile per CTA: no division
+      int tile = p.per_cta == p.KB ? b : b0 / p.KB, kb = b0 - tile * p.KB;
       TileCoord tc = decode_tile<MT, BN, GROUPED>(p, tile, nullptr);
       for (int r = 0; r < pre; ++r) {
         mbar_arrive_expect_tx(&full[r], C::STAGE);
@@ -1089,7 +1095,8 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       const int b1 = range_begin(p, blockIdx.x + 1, gridDim.x);
       const int pre = min(b1 - b0, SR);
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
-      int tile = b0 / p.KB, kb = b0 - tile * p.KB;
+      // one whole tile per CTA: no division
+      int tile = p.per_cta == p.KB ? int(blockIdx.x) : b0 / p.KB, kb = b0 - tile * p.KB;
       TileCoord tc = decode_tile<MT, 128, GROUPED>(p, tile, nullptr);
       for (int r = 0; r < pre; ++r) {
         mbar_arrive_expect_tx(&raw_full[r], uint32_t(C::W_BYTES + um::x_box_rows<MT>(tc.rows) * kBK));
