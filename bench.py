@@ -421,7 +421,8 @@ def run_fq(args, rank, world, local_rank):
         # compute term of the roofline kernel: 2MNK per launch against the engine it runs on
         ops = sum(2.0 * M * big[0] * big[1] for M in MS) / len(MS)
         eng = ep.get("mma_sync_f16_m16n8k16")
-        roofline["compute"] = {"ops_per_launch": ops, "engine": "mma.sync f16 (M<=32) / tcgen05 kind::f16 (M=64)",
+        roofline["compute"] = {"ops_per_launch": ops, "engine": "mma.sync f16 (M<=16) / tcgen05 kind::f16 (M=32,64); "
+                               "peak: the mma.sync f16 one (the lower)",
                                "engine_peak_tflops": eng,
                                "achieved_tflops": round(ops / (dom_ms * 1e-3 / len(MS)) / 1e12, 2),
                                "frac": round(ops / (dom_ms * 1e-3 / len(MS)) / 1e12 / eng, 4) if eng else None}
