@@ -112,6 +112,7 @@ struct Problem {
   int ahead;                // stages the producer keeps in flight (0: the whole ring)
   int w_reuse;              // weight tiles are read by more than one token tile
   int E;                    // grouped: experts
+  int pre_w;                // dense: weight stages issued before the wait on the previous kernel (0: all ahead)
   const float* sx;          // [M] or [R]
   const float* sw;          // [N] or [E, N]
   uint16_t* y;              // [M, N] or [R, N]
@@ -123,7 +124,7 @@ struct Problem {
   int8_t* xq_out;           // ... optional copy of the quantized activations [M, K]
   float* sx_out;            // ... optional copy of their scales [M]
 };
-static_assert(offsetof(Problem, sx) == 48, "producer set-up fields within the first 64 bytes");
+static_assert(offsetof(Problem, sx) <= 56, "producer set-up fields within the first 64 bytes");
 
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -278,6 +279,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
       // this CTA's stream-K range, as rb[] below tabulates it
       const int b0 = range_begin(p, b, G), b1 = range_begin(p, b + 1, G);
       pre = min(b1 - b0, p.ahead > 0 && p.ahead < S ? p.ahead : S);
+      if (p.pre_w > 0 && p.pre_w < pre) pre = p.pre_w;
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       // one whole tile per CTA: no division
       int tile = p.per_cta == p.KB ? b : b0 / p.KB, kb = b0 - tile * p.KB;
@@ -358,6 +360,9 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
       // ones land sooner and the consumers start while the rest stream
       const int AH = p.ahead > 0 && p.ahead < S ? p.ahead : S;
       const int npre = n_it < AH ? n_it : AH;
+      // weight stages issued at kernel entry (the rest of the first AH go out
+      // right after the wait, into ring slots not yet used)
+      const int pre_w = (!GROUPED && p.pre_w > 0 && p.pre_w < npre) ? p.pre_w : npre;
       // weights do not depend on the previous kernel: issue them first
       // (dense problems issued them at kernel entry)
       if (GROUPED) {
@@ -378,7 +383,11 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
       int issued = 0;
       for (int r = 0; r < n_it; ++r) {
         const int s = r % S;
-        if (r < npre) {
+        if (r < pre_w) {
+          if (!FQ) tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
+        } else if (r < npre) {
+          mbar_arrive_expect_tx(&full[s], C::STAGE);
+          tma_load_2d(stages + s * C::STAGE, &tmW, &full[s], kb * kBK, tc.w_row, pol_w);
           if (!FQ) tma_load_2d(stages + s * C::STAGE + C::W_BYTES, &tmX, &full[s], kb * kBK, tc.x_row, pol_x);
         } else {
           // iteration r - AH consumed: at most AH stages in flight, and (as
@@ -1093,7 +1102,7 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       // this CTA's stream-K range, as rb[] below tabulates it
       const int b0 = range_begin(p, blockIdx.x, gridDim.x);
       const int b1 = range_begin(p, blockIdx.x + 1, gridDim.x);
-      const int pre = min(b1 - b0, SR);
+      const int pre = min(b1 - b0, p.pre_w > 0 && p.pre_w < SR ? p.pre_w : SR);
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       // one whole tile per CTA: no division
       int tile = p.per_cta == p.KB ? int(blockIdx.x) : b0 / p.KB, kb = b0 - tile * p.KB;
@@ -1183,6 +1192,9 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       const int npre = n_it < SR ? n_it : SR;
+      // weight stages issued at kernel entry; the other first-lap stages go
+      // out right after the wait, into ring slots not yet used
+      const int pre_w = (!GROUPED && p.pre_w > 0 && p.pre_w < npre) ? p.pre_w : npre;
       auto xrows = [&](int rows) { return um::x_box_rows<MT>(rows); };
       auto load_x = [&](int s_, int kb_, const TileCoord& t_) {
         const int xr = xrows(t_.rows);
@@ -1207,10 +1219,10 @@ __global__ void __launch_bounds__(um::kThreads, 1)
       int issued = 0;
       for (int r = 0; r < n_it; ++r) {
         const int s = r % SR;
-        if (r < npre) {
+        if (r < pre_w) {
           load_x(s, kb, tc);
         } else {
-          if (s_abort || !mbar_wait(&raw_empty[s], uint32_t((r / SR - 1) & 1))) {
+          if (r >= npre && (s_abort || !mbar_wait(&raw_empty[s], uint32_t((r / SR - 1) & 1)))) {
             if (!s_abort) atomicOr(p.err, DEVERR_TIMEOUT);
             s_abort = 1;
             break;
@@ -1660,9 +1672,23 @@ static bool quant_in_gemm(int64_t M, int64_t K, int64_t N, const DevInfo& d) {
   return tiles224 <= d.sm_count && tiles224 * 4 >= int64_t(d.sm_count) * 3;
 }
 
+// Weight stages a dense GEMM issues before its wait on the previous kernel.
+// Copies issued early sit ahead of everything the kernel requests after the
+// wait, so the right number depends on what comes then.  Measured on GB300
+// (K=1024, N=32768, chained calls): the 224-row kernel keeps its whole
+// in-flight window (4 stages) when the previous kernel is another GEMM, but
+// behind the per-token quant - its own, in the one-launch fused op, or the
+// fused op's separate quant launch - one stage is best: M <= 8 fused 8.7-9.4
+// -> 7.9-8.7 us, M = 16 fused 11.2 -> 10.7.  The tcgen05 kernel takes three
+// of its eight raw stages either way: M = 32 10.6 -> 10.1 us, M = 64 11.9 ->
+// 11.7, fused 12.4 -> 11.9 and 14.0 -> 13.7.  The small linear's cluster
+// kernel keeps all of its stages (fewer measured slower at M <= 16).
+constexpr int kPreWaitAfterQuant = 1;
+constexpr int kPreWaitUmma = 3;
+
 fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K, const int8_t* w_nk, const float* sw,
                          int64_t N, uint16_t* y, uint32_t* counters, void* slots, size_t slots_avail, cudaStream_t s,
-                         const DevInfo& d) {
+                         const DevInfo& d, bool after_quant) {
   const int mt = pick_mt(M);
   const int64_t m_tiles = (M + mt - 1) / mt;
   const int KB = int((K + kBK - 1) / kBK);
@@ -1763,6 +1789,7 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     if (g > 0 && g <= grid) grid = g;
   }
   p.per_cta = p.total % grid == 0 ? int(p.total / grid) : 0;
+  p.pre_w = umma ? kPreWaitUmma : (after_quant ? kPreWaitAfterQuant : 0);
   debug_schedule("w8a8_linear", M, K, N, mt_run, data_parallel ? "dp224" : (umma ? "umma" : "streamk"), grid);
   const bool pdl = pdl_enabled();
   cudaError_t e;
@@ -1816,7 +1843,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_linear(const in
   if (!aligned16(ws)) return FQ_ERR_ALIGN;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   return run_w8a8_dense(xq, sx, M, K, w_nk, sw, N, y, reinterpret_cast<uint32_t*>(w8), w8 + kCounterBytes,
-                        ws_bytes - kCounterBytes, reinterpret_cast<cudaStream_t>(stream), d);
+                        ws_bytes - kCounterBytes, reinterpret_cast<cudaStream_t>(stream), d, false);
 }
 
 extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(const uint16_t* x, int64_t M, int64_t K, const int8_t* w_nk, const float* sw,
@@ -1854,6 +1881,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
     p.n_tiles = int(tiles);
     p.total = tiles * p.KB;
     p.per_cta = p.KB;  // one whole tile per CTA
+    p.pre_w = kPreWaitAfterQuant;  // the CTA's own quant comes right after the wait
     p.sw = sw;
     p.y = y;
     p.counters = reinterpret_cast<uint32_t*>(w8);
@@ -1873,7 +1901,7 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
   if (N == 0) return FQ_OK;
   if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, size_t(M) * size_t(N) * 2, s));
   return run_w8a8_dense(xq, sx, M, K, w_nk, sw, N, y, reinterpret_cast<uint32_t*>(w8),
-                        w8 + kCounterBytes + xq_b + sx_b, ws_bytes - kCounterBytes - xq_b - sx_b, s, d);
+                        w8 + kCounterBytes + xq_b + sx_b, ws_bytes - kCounterBytes - xq_b - sx_b, s, d, true);
 }
 
 extern "C" __attribute__((visibility("default"))) fq_status w8a8_grouped_linear(const int8_t* xq, const float* sx, const int32_t* offsets, int64_t R,
@@ -2001,5 +2029,5 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_linear_noalloc(
   cudaError_t e = cudaMemsetAsync(base, 0, size_t(tiles) * 4, s);
   if (e != cudaSuccess) return cuda_status(e);
   return run_w8a8_dense(xq, sx, M, K, w_nk, sw, N, y, reinterpret_cast<uint32_t*>(base), base + noalloc::kCountersNA,
-                        noalloc::kSlotsNA, s, d);
+                        noalloc::kSlotsNA, s, d, false);
 }
