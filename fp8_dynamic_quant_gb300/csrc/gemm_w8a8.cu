@@ -750,10 +750,18 @@ struct CCfg {
   static constexpr int NT = MT / 8;
   static constexpr int BN = 16 * RB;               // RB blocks of 16 weight rows
   static constexpr int CW = RB * KS;               // consumer warps
-  static constexpr int THREADS = (CW + 1) * 32;
+  // Token tiles of 32 and more: converter warps turn each stage's int8
+  // activations into f16 B fragments once (the 224-row kernel's layout), in
+  // place of every consumer widening the fragments of its k-split itself -
+  // RB times over, on its MMA chain (measured with that widening removed:
+  // K=4096, N=1024, M=32 6.0 -> 5.2 us, M=64 8.9 -> 7.0).
+  static constexpr bool CONV = MT >= 32;
+  static constexpr int XW = CONV ? 4 : 0;  // converter warps, each taking every fourth (half, token group)
+  static constexpr int THREADS = (CW + 1 + XW) * 32;
   static constexpr int W_BYTES = BN * kBK;
   static constexpr int X_BYTES = MT * kBK;
   static constexpr int STAGE = W_BYTES + X_BYTES;
+  static constexpr int XF = CONV ? MT * kBK * 2 : 0;  // f16 fragments of a stage
   static constexpr int RECV = CL * KS * 8 * MT * 4;  // [CL ranks][KS k-splits][8 rows][MT tokens] int32
   // Token tiles of up to 16: at most ~100 KB, so that two CTAs fit on an SM
   // (with at most 113 registers a thread) and a call's CTAs can start - and
@@ -762,12 +770,13 @@ struct CCfg {
   // us).  Larger tiles keep one CTA per SM and the deeper ring (at 64 tokens
   // the two-per-SM form measured 10.6 against 9.2 us).
   static constexpr int MINB = MT <= 16 ? 2 : 1;
-  static constexpr int STAGES_FIT = ((MINB == 2 ? 100 : 212) * 1024 - RECV - 2048) / STAGE;
+  static constexpr int STAGES_FIT = ((MINB == 2 ? 100 : 212) * 1024 - RECV - 2048) / (STAGE + XF);
   static constexpr int STAGES = STAGES_FIT > (MINB == 2 ? 12 : 16) ? (MINB == 2 ? 12 : 16) : STAGES_FIT;
-  static constexpr int SMEM = STAGES * STAGE + RECV + 2 * STAGES * 8 + 64 + 1024;
+  static constexpr int SMEM = STAGES * (STAGE + XF) + RECV + 3 * STAGES * 8 + 64 + 1024;
   static_assert(BN == 8 * CL, "each cluster rank owns 8 rows");
   static_assert(KS == 1 || KS == 2 || KS == 4, "k16 steps of a k-block per warp: 8, 4 or 2");
   static_assert(STAGES >= 2, "pipeline too shallow");
+  static_assert(!CONV || KS >= 2, "with the converter a warp takes one or both 16-byte fragment pieces of a half");
 };
 
 template <int MT, int RB, int CL, int KS>
@@ -778,9 +787,11 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  int32_t* recv = reinterpret_cast<int32_t*>(smem + S * C::STAGE);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::STAGE + C::RECV);
+  uint8_t* xfrag = smem + S * C::STAGE;  // CONV: [S][h][NT][2][32 lanes] x 16 bytes of f16 B fragments
+  int32_t* recv = reinterpret_cast<int32_t*>(xfrag + S * C::XF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(xfrag + S * C::XF + C::RECV);
   uint64_t* empty = full + S;
+  uint64_t* xready = empty + S;  // CONV: the stage's fragments are written
   __shared__ int s_issued, s_consumed;
   __shared__ volatile int s_abort;
 
@@ -799,6 +810,7 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kCW);
+      if (C::CONV) mbar_init(&xready[i], C::XW);
     }
     fence_barrier_init();
     s_issued = 0;
@@ -851,6 +863,50 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
     }
     __syncwarp();
     cluster_wait_acquire();  // matches the consumers' wait before their scatter
+  } else if (C::CONV && warp > kCW) {
+    // ------------------------------------------------ activation converters
+    // Converter warp cw takes the (half h, token group j) tasks t = h * NT + j
+    // with t % XW == cw.  Lane l converts what consumer lane l reads: the f16
+    // pairs of its 16-byte chunk, words 0-1 into one 512-byte piece and words
+    // 2-3 into the next.  Rows past M were filled with zeros by the copy.
+    const int cw = warp - kCW - 1;
+    const int g = lane >> 2, c = lane & 3;
+    const int rg = frag_row(g);
+    const uint32_t sbase = smem_u32(stages), xbase = smem_u32(xfrag);
+    for (int r = 0; r < n_it; ++r) {
+      const int s = r % S;
+      if (!mbar_wait_try_first(&full[s], uint32_t((r / S) & 1), &s_abort)) {
+        if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      const uint32_t st = sbase + uint32_t(s * C::STAGE + C::W_BYTES);
+      const uint32_t xo = xbase + uint32_t(s * C::XF) + uint32_t(lane * 16);
+      constexpr int XW = C::XW > 0 ? C::XW : 1;  // (the branch is compiled for every MT)
+      static_assert(!C::CONV || (2 * NT) % XW == 0, "whole tasks per converter warp");
+      uint4 v[2 * NT / XW];
+#pragma unroll
+      for (int i = 0; i < 2 * NT / XW; ++i) {
+        const int t = cw + i * XW, h = t / NT, j = t % NT;
+        v[i] = lds128(st + uint32_t((8 * j + rg) * kBK) + uint32_t(((4 * h + c) ^ rg) << 4));
+      }
+#pragma unroll
+      for (int i = 0; i < 2 * NT / XW; ++i) {
+        const int t = cw + i * XW;
+        uint32_t f[8];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) i8x4_to_f16(word_of(v[i], ks), f[2 * ks], f[2 * ks + 1]);
+        const uint32_t o = xo + uint32_t(t * 2 * 512);
+        sts128(o, f[0], f[1], f[2], f[3]);
+        sts128(o + 512, f[4], f[5], f[6], f[7]);
+      }
+      // generic-proxy reads of the stage before the async-proxy refill
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xready[s]);
+    }
+    __syncwarp();
+    cluster_wait_acquire();  // matches the consumers' wait before their scatter
   } else {
     pdl_wait();
     pdl_launch_dependents();
@@ -874,7 +930,7 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
         for (int a = 0; a < NACC; ++a) accf[a][j][r] = 0.f;
         acci[j][r] = 0;
       }
-    const uint32_t sbase = smem_u32(stages);
+    const uint32_t sbase = smem_u32(stages), xbase = smem_u32(xfrag);
     const uint32_t rowW0 = uint32_t((16 * rbk + rg) * kBK), rowW1 = rowW0 + 8 * kBK;
     const int rows_cur = tc.rows;
     int nk = 0, consumed = 0;
@@ -892,21 +948,35 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
     };
     for (int r = 0; r < n_it; ++r) {
       const int s = r % S;
-      bool ok = mbar_wait_try_first(&full[s], uint32_t((r / S) & 1), &s_abort);
+      const uint32_t par = uint32_t((r / S) & 1);
+      bool ok = mbar_wait_try_first(&full[s], par, &s_abort) &&
+                (!C::CONV || mbar_wait_try_first(&xready[s], par, &s_abort));
       if (!ok) {
         if (!s_abort && lane == 0) atomicOr(p.err, DEVERR_TIMEOUT);
         s_abort = 1;
       }
       const uint32_t st = sbase + uint32_t(s * C::STAGE);
+      const uint32_t xo = xbase + uint32_t(s * C::XF) + uint32_t(lane * 16);
 #pragma unroll
       for (int hh = 0; hh < NH && ok; ++hh) {
         const int h = h0 + hh;
         const uint32_t q = uint32_t(((4 * h + c) ^ rg) << 4);
-        uint32_t wa[NW], wb[NW], wx[NT][NW];
+        uint32_t wa[NW], wb[NW], wx[C::CONV ? 1 : NT][NW];
+        uint4 bx[C::CONV ? NT : 1][NW / 2];  // CONV: the fragment pieces of this warp's words
         pick(lds128(st + rowW0 + q), wa);
         pick(lds128(st + rowW1 + q), wb);
+        if constexpr (C::CONV) {
+          // words 0-1 of the chunk are piece 0, words 2-3 piece 1
 #pragma unroll
-        for (int j = 0; j < NT; ++j) pick(lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q), wx[j]);
+          for (int j = 0; j < NT; ++j)
+            if (8 * j < rows_cur)
+#pragma unroll
+              for (int pc = 0; pc < NW / 2; ++pc)
+                bx[j][pc] = lds128(xo + uint32_t(((h * NT + j) * 2 + (NW == 4 ? pc : (hi_words ? 1 : 0))) * 512));
+        } else {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) pick(lds128(st + C::W_BYTES + uint32_t((8 * j + rg) * kBK) + q), wx[j]);
+        }
 #pragma unroll
         for (int ks = 0; ks < NW; ++ks) {
           uint32_t a0, a1, a2, a3;
@@ -916,7 +986,13 @@ __global__ void __launch_bounds__(CCfg<MT, RB, CL, KS>::THREADS, CCfg<MT, RB, CL
           for (int j = 0; j < NT; ++j) {
             if (8 * j < rows_cur) {
               uint32_t b0, b1;
-              i8x4_to_f16(wx[j][ks], b0, b1);
+              if constexpr (C::CONV) {
+                const uint4& v = bx[j][NW == 4 ? (ks >> 1) : 0];
+                b0 = word_of(v, 2 * (ks & 1));
+                b1 = word_of(v, 2 * (ks & 1) + 1);
+              } else {
+                i8x4_to_f16(wx[j][ks], b0, b1);
+              }
               mma_f16(accf[(NH == 2 ? hh : ks) % NACC][j], a0, a1, a2, a3, b0, b1);
             }
           }
