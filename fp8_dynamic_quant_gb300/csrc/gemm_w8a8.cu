@@ -463,36 +463,47 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
     pdl_launch_dependents();
     if constexpr (FQ) {
       // Per-token quant of the whole activation tile (one tile per CTA, all of
-      // K), one row per warp, with the quant kernel's arithmetic: the warp's
-      // max is the row's absmax whatever the order, so the scale and codes
-      // are the quant kernel's bit for bit.  CTA 0 also writes the optional
-      // copies.  Meanwhile the first weight stages are still in flight.
+      // K), rows m = warp, warp + kCW, ... per warp, with the quant kernel's
+      // arithmetic: the warp's max is the row's absmax whatever the order, so
+      // the scale and codes are the quant kernel's bit for bit.  A warp's rows
+      // have their loads issued together, before any reduction.  CTA 0 also
+      // writes the optional copies.  Meanwhile the first weight stages are
+      // still in flight.
       const int rows = min(MT, p.M);
       const int K8 = p.K / 8;
-      constexpr int VPL = kFuseKMax / 256;  // 16-byte vectors per lane
+      constexpr int VPL = kFuseKMax / 256;          // 16-byte vectors per lane
+      constexpr int RPW = (MT + kCW - 1) / kCW;     // rows per warp
       const uint32_t xqbase = smem_u32(xqs);
-      for (int m = warp; m < rows; m += kCW) {
+      uint4 v[RPW][VPL];
+      float amax[RPW];
+#pragma unroll
+      for (int u = 0; u < RPW; ++u) {
+        const int m = warp + u * kCW;
         const uint4* xr = reinterpret_cast<const uint4*>(p.x16) + int64_t(m) * K8;
-        uint4 v[VPL];
-        float amax = 0.0f;
+        amax[u] = 0.0f;
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int idx = lane + 32 * i;
-          if (idx < K8) {
-            v[i] = ld_stream(xr + idx);
-            amax = fmaxf(amax, absmax8_bf16(v[i]));
+          if (m < rows && idx < K8) {
+            v[u][i] = ld_stream(xr + idx);
+            amax[u] = fmaxf(amax[u], absmax8_bf16(v[u][i]));
           }
         }
+      }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const float sc = __fdiv_rn(amax, 127.0f);
+      for (int u = 0; u < RPW; ++u) {
+        const int m = warp + u * kCW;
+        if (m >= rows) break;  // warp-uniform
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax[u] = fmaxf(amax[u], __shfl_xor_sync(0xFFFFFFFFu, amax[u], o));
+        const float sc = __fdiv_rn(amax[u], 127.0f);
         const float inv = __frcp_rn(sc);
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int idx = lane + 32 * i;
           if (idx < K8) {
             float f[8];
-            unpack8(v[i], f);
+            unpack8(v[u][i], f);
             const uint2 qv = quant8_i8(f, sc, inv);
             const int k = idx * 8;
             const uint32_t a = xqbase + uint32_t(((k >> 7) * MT + m) * kBK + ((((k >> 4) & 7) ^ (m & 7)) << 4) + (k & 8));
@@ -1735,12 +1746,14 @@ static void debug_schedule(const char* op, int64_t M, int64_t K, int64_t N, int 
 // The fused op runs as one launch when the dense schedule would stream one
 // whole 224-row tile per CTA and the whole quantized activation tile fits in
 // shared memory: each CTA quantizes the activations itself, one row per warp,
-// after the previous kernel has finished.  With 8-token tiles that beats a
-// separate quant launch; with 16 some warps take two rows one after the other
-// and the quant (measured) no longer hides under the first weight stages.
+// after the previous kernel has finished.  That beats a separate quant launch
+// while every row has a consumer warp of its own (K=1024, N=32768 on GB300:
+// M=9 10.8 -> 10.6 us); with 15 or 16 rows two warps quantize two rows one
+// after the other (M=16: 11.4 against 10.8 us with two launches).
 static bool quant_in_gemm(int64_t M, int64_t K, int64_t N, const DevInfo& d) {
   const int mt = pick_mt(M);
-  if (mt > 8 || M > mt || K > kFuseKMax) return false;
+  if (mt > 16 || M > mt || K > kFuseKMax) return false;
+  if (M > 14) return false;  // one row per consumer warp of the 224-row kernel
   const int force = forced_schedule();
   const int64_t tiles224 = (N + 223) / 224;
   if (force == SCHED_DP) return tiles224 <= kMaxGrid;
@@ -1970,7 +1983,8 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
     if (!tensor_map_u8_2d(&tw_map, w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, 224u)) return FQ_ERR_CUDA;
     debug_schedule("w8a8_quant_linear", M, K, N, mt, "dp224+quant", int(tiles));
     const bool pdl = pdl_enabled();
-    return cuda_status(launch_gemm<8, 14, false, true>(&tw_map, &tw_map, p, int(tiles), s, pdl));
+    return cuda_status(mt == 8 ? launch_gemm<8, 14, false, true>(&tw_map, &tw_map, p, int(tiles), s, pdl)
+                               : launch_gemm<16, 14, false, true>(&tw_map, &tw_map, p, int(tiles), s, pdl));
   }
   // the quant's output is this call's activations: the GEMM may launch early
   if ((st = quant_int8_launch(x, M, K, xq, sx, stream, true)) != FQ_OK) return st;

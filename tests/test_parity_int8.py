@@ -193,7 +193,9 @@ def test_fused_quant_linear_equals_two_steps(M, K, N):
 # which every CTA quantizes the activations itself.  Ragged K (1008, 144, 16)
 # and N.
 FUSED_ONE_LAUNCH = [(1, 1024, 32768), (2, 1024, 32768), (3, 1024, 25600), (7, 1008, 30000), (8, 1024, 33152),
-                    (6, 512, 29008), (8, 1024, 32768), (5, 16, 26000), (4, 144, 33008)]
+                    (6, 512, 29008), (8, 1024, 32768), (5, 16, 26000), (4, 144, 33008),
+                    # 16-token tiles, one row per consumer warp
+                    (9, 1024, 32768), (14, 1024, 32768), (12, 1008, 30000), (10, 512, 29008), (13, 16, 26000)]
 
 
 def _fused_one_launch(x, w_nk, sw):
@@ -220,12 +222,13 @@ def test_fused_one_launch_bit_exact(M, K, N, monkeypatch, capfd):
     assert np.array_equal(y_plain, want)
 
 
-def test_fused_one_launch_forced_small_n_and_ties(monkeypatch, capfd):
+@pytest.mark.parametrize("M", [8, 14])
+def test_fused_one_launch_forced_small_n_and_ties(M, monkeypatch, capfd):
     """Forced data-parallel schedule on a small N, and rows whose quotients sit at k + 0.5."""
     monkeypatch.setenv("FQ_DEBUG_SCHEDULE", "1")
     monkeypatch.setenv("FQ_FORCE_SCHEDULE", "dp")
-    r = np.random.default_rng(11)
-    M, K, N = 8, 1024, 2240
+    r = np.random.default_rng(11 + M)
+    K, N = 1024, 2240
     amax = 127.0 * 1.5
     rows = []
     for m in range(M):
