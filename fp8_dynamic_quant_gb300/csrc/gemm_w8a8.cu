@@ -256,6 +256,8 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
   uint64_t* empty = full + S;
   uint64_t* xready = empty + S;
   __shared__ float s_sxq[FQ ? MT : 1];
+  __shared__ unsigned s_amax[FQ ? MT : 1];  // FQ: row absmax bits (non-negative floats order as integers)
+  __shared__ float s_inv[FQ ? MT : 1];      // FQ: reciprocal of each row's scale
   __shared__ int s_flag;
   __shared__ int s_issued, s_consumed;
   __shared__ volatile int s_abort;  // set after any timed-out wait: later waits are skipped
@@ -265,6 +267,7 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, b = blockIdx.x;
   const bool producer = warp == kCW && lane == 0;
+  if (FQ && tid < MT) s_amax[tid] = 0u;  // before the first block barrier
   constexpr int kConv = CW + 1;  // the activation-converter warp
   // The producer thread sets up the ring and, for dense problems, issues the
   // first stages of weights before anything else: they depend on nothing, and
@@ -463,57 +466,133 @@ __global__ void __launch_bounds__(Cfg<MT, CW, FQ>::THREADS, 1)
     pdl_launch_dependents();
     if constexpr (FQ) {
       // Per-token quant of the whole activation tile (one tile per CTA, all of
-      // K), rows m = warp, warp + kCW, ... per warp, with the quant kernel's
-      // arithmetic: the warp's max is the row's absmax whatever the order, so
-      // the scale and codes are the quant kernel's bit for bit.  A warp's rows
-      // have their loads issued together, before any reduction.  CTA 0 also
-      // writes the optional copies.  Meanwhile the first weight stages are
-      // still in flight.
+      // K) with the quant kernel's arithmetic; the row max does not depend on
+      // the order, so the scale and codes are the quant kernel's bit for bit.
+      // CTA 0 also writes the optional copies.  Meanwhile the first weight
+      // stages are in flight.
       const int rows = min(MT, p.M);
       const int K8 = p.K / 8;
-      constexpr int VPL = kFuseKMax / 256;          // 16-byte vectors per lane
-      constexpr int RPW = (MT + kCW - 1) / kCW;     // rows per warp
       const uint32_t xqbase = smem_u32(xqs);
-      uint4 v[RPW][VPL];
-      float amax[RPW];
+      if (rows <= 4) {
+        // Few rows: all consumer threads share the tile.  Thread t takes the
+        // 16-byte vectors t, t + kCW * 32, ... of the rows x K/8 vectors;
+        // each warp reduces the row maxima of its 32 consecutive vectors and
+        // posts them with a shared atomicMax on the float bits (non-negative:
+        // a NaN vector counts as 0, as fmaxf ignores it).  GB300, K=1024,
+        // N=32768: M = 1 / 4 8.1 -> 7.9 / 8.8 -> 8.5 us against one row per
+        // warp; from 7 rows on the two consumer barriers cost more than that
+        // saves.
+        const int nvec = rows * K8;
+        constexpr int kCT = kCW * 32;                              // consumer threads
+        constexpr int NV = (4 * (kFuseKMax / 8) + kCT - 1) / kCT;  // vectors per thread, at most (rows <= 4)
+        const uint4* xv = reinterpret_cast<const uint4*>(p.x16);   // rows of K8 vectors, contiguous
+        uint4 v[NV];
 #pragma unroll
-      for (int u = 0; u < RPW; ++u) {
-        const int m = warp + u * kCW;
-        const uint4* xr = reinterpret_cast<const uint4*>(p.x16) + int64_t(m) * K8;
-        amax[u] = 0.0f;
+        for (int i = 0; i < NV; ++i) {
+          const int e = tid + i * kCT;
+          if (e < nvec) v[i] = ld_stream(xv + e);
+        }
+        float a[NV];
+        int row[NV];
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-          const int idx = lane + 32 * i;
-          if (m < rows && idx < K8) {
-            v[u][i] = ld_stream(xr + idx);
-            amax[u] = fmaxf(amax[u], absmax8_bf16(v[u][i]));
+        for (int i = 0; i < NV; ++i) {
+          const int e = tid + i * kCT;
+          a[i] = e < nvec ? fmaxf(0.0f, absmax8_bf16(v[i])) : 0.0f;
+          row[i] = (e < nvec ? e : nvec - 1) / K8;
+        }
+        if (K8 % 32 == 0) {
+          // a warp's 32 vectors lie in one row: a butterfly max, the chains interleaved
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < NV; ++i) a[i] = fmaxf(a[i], __shfl_xor_sync(0xFFFFFFFFu, a[i], o));
+#pragma unroll
+          for (int i = 0; i < NV; ++i)
+            if (lane == 0 && i * kCT + warp * 32 < nvec) atomicMax(&s_amax[row[i]], __float_as_uint(a[i]));
+        } else {
+          // rows shorter than a warp's vectors, or not aligned to them: segmented max
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+              const float ao = __shfl_down_sync(0xFFFFFFFFu, a[i], o);
+              const int ro = __shfl_down_sync(0xFFFFFFFFu, row[i], o);
+              if (lane + o < 32 && ro == row[i]) a[i] = fmaxf(a[i], ao);
+            }
+#pragma unroll
+          for (int i = 0; i < NV; ++i) {
+            const int rprev = __shfl_up_sync(0xFFFFFFFFu, row[i], 1);
+            if (tid + i * kCT < nvec && (lane == 0 || rprev != row[i])) atomicMax(&s_amax[row[i]], __float_as_uint(a[i]));
           }
         }
-      }
+        named_bar_sync(3, kCT);
+        if (tid < rows) {
+          const float sc = __fdiv_rn(__uint_as_float(s_amax[tid]), 127.0f);
+          s_sxq[tid] = sc;
+          s_inv[tid] = __frcp_rn(sc);
+          if (b == 0 && p.sx_out) p.sx_out[tid] = sc;
+        }
+        named_bar_sync(3, kCT);
 #pragma unroll
-      for (int u = 0; u < RPW; ++u) {
-        const int m = warp + u * kCW;
-        if (m >= rows) break;  // warp-uniform
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax[u] = fmaxf(amax[u], __shfl_xor_sync(0xFFFFFFFFu, amax[u], o));
-        const float sc = __fdiv_rn(amax[u], 127.0f);
-        const float inv = __frcp_rn(sc);
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-          const int idx = lane + 32 * i;
-          if (idx < K8) {
+        for (int i = 0; i < NV; ++i) {
+          const int e = tid + i * kCT;
+          if (e < nvec) {
+            const int m = row[i], idx = e - m * K8;
             float f[8];
-            unpack8(v[u][i], f);
-            const uint2 qv = quant8_i8(f, sc, inv);
+            unpack8(v[i], f);
+            const uint2 qv = quant8_i8(f, s_sxq[m], s_inv[m]);
             const int k = idx * 8;
-            const uint32_t a = xqbase + uint32_t(((k >> 7) * MT + m) * kBK + ((((k >> 4) & 7) ^ (m & 7)) << 4) + (k & 8));
-            asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(a), "r"(qv.x), "r"(qv.y) : "memory");
+            const uint32_t sa = xqbase + uint32_t(((k >> 7) * MT + m) * kBK + ((((k >> 4) & 7) ^ (m & 7)) << 4) + (k & 8));
+            asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(sa), "r"(qv.x), "r"(qv.y) : "memory");
             if (b == 0 && p.xq_out) *reinterpret_cast<uint2*>(p.xq_out + int64_t(m) * p.K + k) = qv;
           }
         }
-        if (lane == 0) {
-          s_sxq[m] = sc;
-          if (b == 0 && p.sx_out) p.sx_out[m] = sc;
+      } else {
+        // One row per warp (rows m = warp, warp + kCW, ...; a warp's loads
+        // issued before its reductions).
+        constexpr int VPL = kFuseKMax / 256;       // 16-byte vectors per lane
+        constexpr int RPW = (MT + kCW - 1) / kCW;  // rows per warp
+        uint4 v[RPW][VPL];
+        float amax[RPW];
+#pragma unroll
+        for (int u = 0; u < RPW; ++u) {
+          const int m = warp + u * kCW;
+          const uint4* xr = reinterpret_cast<const uint4*>(p.x16) + int64_t(m) * K8;
+          amax[u] = 0.0f;
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) {
+            const int idx = lane + 32 * i;
+            if (m < rows && idx < K8) {
+              v[u][i] = ld_stream(xr + idx);
+              amax[u] = fmaxf(amax[u], absmax8_bf16(v[u][i]));
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < RPW; ++u) {
+          const int m = warp + u * kCW;
+          if (m >= rows) break;  // warp-uniform
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) amax[u] = fmaxf(amax[u], __shfl_xor_sync(0xFFFFFFFFu, amax[u], o));
+          const float sc = __fdiv_rn(amax[u], 127.0f);
+          const float inv = __frcp_rn(sc);
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) {
+            const int idx = lane + 32 * i;
+            if (idx < K8) {
+              float f[8];
+              unpack8(v[u][i], f);
+              const uint2 qv = quant8_i8(f, sc, inv);
+              const int k = idx * 8;
+              const uint32_t sa = xqbase + uint32_t(((k >> 7) * MT + m) * kBK + ((((k >> 4) & 7) ^ (m & 7)) << 4) + (k & 8));
+              asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(sa), "r"(qv.x), "r"(qv.y) : "memory");
+              if (b == 0 && p.xq_out) *reinterpret_cast<uint2*>(p.xq_out + int64_t(m) * p.K + k) = qv;
+            }
+          }
+          if (lane == 0) {
+            s_sxq[m] = sc;
+            if (b == 0 && p.sx_out) p.sx_out[m] = sc;
+          }
         }
       }
       named_bar_sync(2, (kCW + 1) * 32);  // with the converter warp
@@ -1745,11 +1824,11 @@ static void debug_schedule(const char* op, int64_t M, int64_t K, int64_t N, int 
 // counter block at the head of the workspace; `slots` the partial-sum area.
 // The fused op runs as one launch when the dense schedule would stream one
 // whole 224-row tile per CTA and the whole quantized activation tile fits in
-// shared memory: each CTA quantizes the activations itself, one row per warp,
-// after the previous kernel has finished.  That beats a separate quant launch
-// while every row has a consumer warp of its own (K=1024, N=32768 on GB300:
-// M=9 10.8 -> 10.6 us); with 15 or 16 rows two warps quantize two rows one
-// after the other (M=16: 11.4 against 10.8 us with two launches).
+// shared memory: each CTA quantizes the activations itself after the previous
+// kernel has finished.  That beats a separate quant launch while every row
+// has a consumer warp of its own (K=1024, N=32768 on GB300: M=9 10.8 -> 10.4
+// us); with 15 or 16 rows two warps quantize two rows one after the other
+// (M=16: 11.4 against 10.7 us with two launches).
 static bool quant_in_gemm(int64_t M, int64_t K, int64_t N, const DevInfo& d) {
   const int mt = pick_mt(M);
   if (mt > 16 || M > mt || K > kFuseKMax) return false;

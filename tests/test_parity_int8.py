@@ -195,7 +195,8 @@ def test_fused_quant_linear_equals_two_steps(M, K, N):
 FUSED_ONE_LAUNCH = [(1, 1024, 32768), (2, 1024, 32768), (3, 1024, 25600), (7, 1008, 30000), (8, 1024, 33152),
                     (6, 512, 29008), (8, 1024, 32768), (5, 16, 26000), (4, 144, 33008),
                     # 16-token tiles, one row per consumer warp
-                    (9, 1024, 32768), (14, 1024, 32768), (12, 1008, 30000), (10, 512, 29008), (13, 16, 26000)]
+                    (9, 1024, 32768), (14, 1024, 32768), (12, 1008, 30000), (10, 512, 29008), (13, 16, 26000),
+                    (11, 144, 33008)]
 
 
 def _fused_one_launch(x, w_nk, sw):
@@ -222,7 +223,7 @@ def test_fused_one_launch_bit_exact(M, K, N, monkeypatch, capfd):
     assert np.array_equal(y_plain, want)
 
 
-@pytest.mark.parametrize("M", [8, 14])
+@pytest.mark.parametrize("M", [1, 3, 8, 14])
 def test_fused_one_launch_forced_small_n_and_ties(M, monkeypatch, capfd):
     """Forced data-parallel schedule on a small N, and rows whose quotients sit at k + 0.5."""
     monkeypatch.setenv("FQ_DEBUG_SCHEDULE", "1")
