@@ -1843,14 +1843,16 @@ static bool quant_in_gemm(int64_t M, int64_t K, int64_t N, const DevInfo& d) {
 // Weight stages a dense GEMM issues before its wait on the previous kernel.
 // Copies issued early sit ahead of everything the kernel requests after the
 // wait, so the right number depends on what comes then.  Measured on GB300
-// (K=1024, N=32768, chained calls): the 224-row kernel keeps its whole
-// in-flight window (4 stages) when the previous kernel is another GEMM, but
+// (K=1024, N=32768, chained calls): the 224-row kernel takes three of its
+// four in-flight stages when the previous kernel is another GEMM (M <= 8
+// 7.85 -> 7.75 us, M = 16 9.1 -> 9.0; one or two stages are slower), but
 // behind the per-token quant - its own, in the one-launch fused op, or the
-// fused op's separate quant launch - one stage is best: M <= 8 fused 8.7-9.4
-// -> 7.9-8.7 us, M = 16 fused 11.2 -> 10.7.  The tcgen05 kernel takes three
+// fused op's separate quant launch - one stage: M <= 8 fused 8.7-9.4 ->
+// 7.9-8.7 us, M = 16 fused 11.2 -> 10.7.  The tcgen05 kernel takes three
 // of its eight raw stages either way: M = 32 10.6 -> 10.1 us, M = 64 11.9 ->
 // 11.7, fused 12.4 -> 11.9 and 14.0 -> 13.7.  The small linear's cluster
 // kernel keeps all of its stages (fewer measured slower at M <= 16).
+constexpr int kPreWaitAfterGemm = 3;
 constexpr int kPreWaitAfterQuant = 1;
 constexpr int kPreWaitUmma = 3;
 
@@ -1957,7 +1959,8 @@ fq_status run_w8a8_dense(const int8_t* xq, const float* sx, int64_t M, int64_t K
     if (g > 0 && g <= grid) grid = g;
   }
   p.per_cta = p.total % grid == 0 ? int(p.total / grid) : 0;
-  p.pre_w = umma ? kPreWaitUmma : (after_quant ? kPreWaitAfterQuant : 0);
+  // (measured on the whole-tile schedules; the stream-K mma.sync form keeps its default)
+  p.pre_w = umma ? kPreWaitUmma : (data_parallel ? (after_quant ? kPreWaitAfterQuant : kPreWaitAfterGemm) : 0);
   debug_schedule("w8a8_linear", M, K, N, mt_run, data_parallel ? "dp224" : (umma ? "umma" : "streamk"), grid);
   const bool pdl = pdl_enabled();
   cudaError_t e;
