@@ -26,8 +26,9 @@
 //    contiguous 16-byte chunk per row and the same physical-to-logical K
 //    permutation is applied to both operands, so no shuffles are needed.
 //  * Small N (K=4096, N=1024): 4-CTA clusters split K and reduce through
-//    distributed shared memory; 64-token tiles on wide N and the MoE: the
-//    tcgen05 kernel below.
+//    distributed shared memory (with converter warps for token tiles of 32
+//    and 64); 32- and 64-token tiles on wide N and the MoE: the tcgen05
+//    kernel below.
 //  * Scheduling: stream-K.  The (tile, k-block) iteration space is cut into
 //    equal contiguous ranges, one per CTA (one CTA per SM), which balances
 //    any (M, N, K) across all 152 SMs - the role the pages give to baseM /
@@ -36,14 +37,15 @@
 //    per-CTA workspace slots, and the last CTA to finish a tile (counted with
 //    an atomic per tile) adds them up and runs the dequant epilogue.  Integer
 //    sums make the result independent of that order.  When 224-row tiles
-//    give 3/4 to 1 tile per SM (up to 32 tokens), each CTA streams one whole
-//    tile instead, and the fused op with up to 8 tokens is one launch whose
+//    give 3/4 to 1 tile per SM (up to 16 tokens), each CTA streams one whole
+//    tile instead, and the fused op with up to 14 tokens is one launch whose
 //    CTAs quantize the activations themselves.
 //  * Weights are read with an L2 evict-first hint; activations evict-last.
 //  * Programmatic dependent launch: weight loads for the first stages are
 //    issued at kernel entry, before griddepcontrol.wait, overlapping the
-//    previous kernel.  (Library calls that can write a weight operand let
-//    the next kernel start only once they have finished.)
+//    previous kernel - how many, the host picks by what the kernel requests
+//    right after the wait.  (Library calls that can write a weight operand
+//    let the next kernel start only once they have finished.)
 #include <cuda_fp16.h>
 
 #include <cstddef>
