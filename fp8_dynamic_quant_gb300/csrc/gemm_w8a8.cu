@@ -2063,6 +2063,12 @@ extern "C" __attribute__((visibility("default"))) fq_status w8a8_quant_linear(co
     p.xq_out = xq_out;
     p.sx_out = sx_out;
     p.ahead = stages_ahead(224 * kBK);
+    // With 3 to 8 rows the CTA's own quant holds its consumers back for a
+    // while after the wait; one more stage in flight keeps the weight stream
+    // going meanwhile (GB300, K=1024, N=32768: M = 3 / 4 / 7 / 8 8.1 / 8.3 /
+    // 8.35 / 8.7 -> 7.7 / 7.75 / 7.8 / 8.2 us; with 1 or 2 rows, or 16-token
+    // tiles, the window of the plain GEMM measured as fast or faster).
+    if (mt == 8 && M >= 3 && !std::getenv("FQ_STAGES_AHEAD")) p.ahead += 1;
     CUtensorMap tw_map;
     if (!tensor_map_u8_2d(&tw_map, w_nk, uint64_t(K), uint64_t(N), uint64_t(K), kBK, 224u)) return FQ_ERR_CUDA;
     debug_schedule("w8a8_quant_linear", M, K, N, mt, "dp224+quant", int(tiles));
