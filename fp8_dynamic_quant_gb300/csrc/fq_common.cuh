@@ -433,10 +433,34 @@ __device__ __forceinline__ float absmax8(const float f[8]) {
   return m;
 }
 
-// max(a, |b|) propagating NaN (PTX max.NaN): a NaN anywhere reaches the result.
-__device__ __forceinline__ float max_abs_nan(float a, float b) {
+// Packed fp32 pairs (Blackwell's f32x2 multiply, add and subtract): each half
+// is the IEEE round-to-nearest-even result, subnormals kept, the same value
+// as the scalar __fmul_rn / __fadd_rn / __fsub_rn; one instruction for two.
+__device__ __forceinline__ float2 f2_op_mul(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_op_add(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_op_sub(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+      : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// max(a, |b|, |c|) propagating NaN (three-input PTX max.NaN).
+__device__ __forceinline__ float max_abs2_nan(float a, float b, float c) {
   float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(fabsf(b)));
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(fabsf(b)), "f"(fabsf(c)));
   return r;
 }
 
@@ -447,20 +471,23 @@ __device__ __forceinline__ float max_abs_nan(float a, float b) {
 // decide for all eight at once: if any lies within 2^-14 of a half-integer,
 // rounds beyond +-127 (the clamp) or is not a number (s == 0, RN(1/s) not
 // finite, a NaN or infinite input), all eight take the exact per-element
-// path.  Identical codes, about a third of the per-element path's
-// instructions (the kernel was issue-bound on GB300).
+// path.  The fast path works on pairs (f32x2) and three-input maxima.
+// Identical codes, a fraction of the per-element path's instructions (the
+// many-rows kernel is issue-bound on GB300).
 __device__ __forceinline__ uint2 quant8_i8(const float f[8], float s, float inv) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const float2 inv2 = make_float2(inv, inv), mg = make_float2(kMagic, kMagic);
   uint32_t t[8];
   float dmax = 0.0f, ymax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float y = __fmul_rn(f[i], inv);
-    const float tm = __fadd_rn(y, kMagic);
-    const float r = __fsub_rn(tm, kMagic);
-    dmax = max_abs_nan(dmax, __fsub_rn(y, r));
-    ymax = max_abs_nan(ymax, y);
-    t[i] = __float_as_uint(tm);
+  for (int i = 0; i < 4; ++i) {
+    const float2 y = f2_op_mul(make_float2(f[2 * i], f[2 * i + 1]), inv2);
+    const float2 tm = f2_op_add(y, mg);
+    const float2 d = f2_op_sub(y, f2_op_sub(tm, mg));
+    dmax = max_abs2_nan(dmax, d.x, d.y);
+    ymax = max_abs2_nan(ymax, y.x, y.y);
+    t[2 * i] = __float_as_uint(tm.x);
+    t[2 * i + 1] = __float_as_uint(tm.y);
   }
   uint2 o;
   if (dmax < 0.5f - 1.0f / 16384.0f && ymax < 127.5f) {
