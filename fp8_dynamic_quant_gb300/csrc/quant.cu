@@ -863,6 +863,21 @@ static int grid_for(int64_t work, int per_cta, int sms, int ctas_per_sm) {
   return int(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
+// CTAs of `kernel` an SM holds at once (registers, threads, shared memory),
+// at most `cap`.  A grid-stride kernel sized to this runs in one wave: a grid
+// of more CTAs than the SMs hold leaves a partial second wave, and the next
+// kernel's early-launched CTAs, parked at their dependency wait, then take
+// the slots that wave needs.
+template <typename Kern>
+static int resident_ctas(Kern kernel, int threads, size_t smem, int cap) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n < cap ? n : cap;
+}
+
 }  // namespace fq
 
 using namespace fq;
@@ -1076,7 +1091,11 @@ static fq_status fp8_group_common(const uint16_t* x, int64_t T, int64_t G, int64
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t units = G * P * (sp ? Ta : T);
   if (units == 0) return FQ_OK;
-  const int grid = grid_for(units, 8, d.sm_count, 8);
+  // one wave (GB300, T=4096, G=8, D=4096: 39 registers hold 6 CTAs per SM)
+  static int occ[2] = {0, 0};
+  int& oc = occ[sp ? 1 : 0];
+  if (!oc) oc = sp ? resident_ctas(quant_fp8_group_kernel<true>, 256, 0, 8) : resident_ctas(quant_fp8_group_kernel<false>, 256, 0, 8);
+  const int grid = grid_for(units, 8, d.sm_count, oc);
   cudaError_t e;
   if (sp)
     e = launch(quant_fp8_group_kernel<true>, grid, 256, 0, s, pdl_enabled(), reinterpret_cast<const uint4*>(x),
@@ -1193,7 +1212,9 @@ extern "C" __attribute__((visibility("default"))) fq_status quant_mxfp8(const ui
   fq_status st = device_info(&d);
   if (st != FQ_OK) return st;
   const int64_t K8 = K / 8;
-  const int grid = grid_for(R * K8, 256, d.sm_count, 8);
+  static int occ = 0;  // one wave
+  if (!occ) occ = resident_ctas(quant_mxfp8_kernel, 256, 0, 8);
+  const int grid = grid_for(R * K8, 256, d.sm_count, occ);
   return cuda_status(launch(quant_mxfp8_kernel, grid, 256, 0, reinterpret_cast<cudaStream_t>(stream), pdl_enabled(),
                             reinterpret_cast<const uint4*>(x), R, K8, reinterpret_cast<uint2*>(q), sf_blocked));
 }
