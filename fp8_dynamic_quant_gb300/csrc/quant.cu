@@ -18,6 +18,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <mutex>
+
 #include "fq_common.cuh"
 
 namespace fq {
@@ -867,15 +869,33 @@ static int grid_for(int64_t work, int per_cta, int sms, int ctas_per_sm) {
 // at most `cap`.  A grid-stride kernel sized to this runs in one wave: a grid
 // of more CTAs than the SMs hold leaves a partial second wave, and the next
 // kernel's early-launched CTAs, parked at their dependency wait, then take
-// the slots that wave needs.
-template <typename Kern>
-static int resident_ctas(Kern kernel, int threads, size_t smem, int cap) {
+// the slots that wave needs.  Cached per (kernel, block size).
+static int resident_ctas(const void* kernel, int threads, int cap) {
+  struct Entry {
+    const void* k;
+    int threads, n;
+  };
+  static Entry tab[64];
+  static int used = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    n = 1;
+  for (int i = 0; i < used && !n; ++i)
+    if (tab[i].k == kernel && tab[i].threads == threads) n = tab[i].n;
+  if (!n) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    if (used < 64) tab[used++] = {kernel, threads, n};
   }
   return n < cap ? n : cap;
+}
+
+// the grid of a grid-stride kernel over `work` units (`per_cta` a CTA at a time), one wave
+template <typename Kern>
+static int wave_grid(Kern kernel, int threads, int64_t work, int per_cta, int sms, int cap) {
+  return grid_for(work, per_cta, sms, resident_ctas(reinterpret_cast<const void*>(kernel), threads, cap));
 }
 
 }  // namespace fq
@@ -1043,12 +1063,15 @@ extern "C" __attribute__((visibility("default"))) fq_status swiglu_quant_int8(co
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t I8 = I / 8;
   const int threads = I8 >= 256 ? 256 : (I8 >= 128 ? 128 : (I8 >= 64 ? 64 : 32));
-  const int grid = grid_for(rows, 1, d.sm_count, 2048 / threads);
   const int64_t vpt = (I8 + threads - 1) / threads;
   const bool pdl = pdl_enabled();
   auto gp = reinterpret_cast<const uint4*>(gu);
   auto qp = reinterpret_cast<uint2*>(hq);
   auto hp = reinterpret_cast<uint4*>(h_out);
+  // More CTAs than the SMs hold at once: one row per CTA at a time, so the
+  // extra rows in flight pay (a one-wave grid measured 20.3 -> 21.6 us at
+  // 2048 rows, I = 2048, on GB300).
+  const int grid = grid_for(rows, 1, d.sm_count, 2048 / threads);
   cudaError_t e;
   if (vpt <= 1)
     e = launch(swiglu_quant_int8_kernel<1>, grid, threads, 0, s, pdl, gp, rows, I8, qp, sh, hp);
@@ -1091,11 +1114,10 @@ static fq_status fp8_group_common(const uint16_t* x, int64_t T, int64_t G, int64
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t units = G * P * (sp ? Ta : T);
   if (units == 0) return FQ_OK;
-  // one wave (GB300, T=4096, G=8, D=4096: 39 registers hold 6 CTAs per SM)
-  static int occ[2] = {0, 0};
-  int& oc = occ[sp ? 1 : 0];
-  if (!oc) oc = sp ? resident_ctas(quant_fp8_group_kernel<true>, 256, 0, 8) : resident_ctas(quant_fp8_group_kernel<false>, 256, 0, 8);
-  const int grid = grid_for(units, 8, d.sm_count, oc);
+  // one wave (GB300, T=4096, G=8, D=4096: 39 registers hold 6 CTAs of 256 per SM;
+  // 8 per SM measured 79.2 against 69.5 us)
+  const int grid = sp ? wave_grid(quant_fp8_group_kernel<true>, 256, units, 8, d.sm_count, 8)
+                      : wave_grid(quant_fp8_group_kernel<false>, 256, units, 8, d.sm_count, 8);
   cudaError_t e;
   if (sp)
     e = launch(quant_fp8_group_kernel<true>, grid, 256, 0, s, pdl_enabled(), reinterpret_cast<const uint4*>(x),
@@ -1163,6 +1185,9 @@ static fq_status rmsnorm_common(const uint16_t* x, const uint16_t* gamma, float 
   const int64_t K8 = K / 8;
   const int64_t rows = fp8 ? (M + 3) / 4 * 4 : M;
   const int P = int((K / 128 + 3) / 4), Ta = int((M + 3) / 4 * 4);
+  // More CTAs than the SMs hold at once: one row per CTA at a time, so the
+  // extra rows in flight pay (a one-wave grid measured 153.4 -> 155.5 us at
+  // M=16384, K=4096, on GB300).
   const int grid = grid_for(rows, 1, d.sm_count, 8);
   const int64_t vpt = (K8 + 255) / 256;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1212,9 +1237,7 @@ extern "C" __attribute__((visibility("default"))) fq_status quant_mxfp8(const ui
   fq_status st = device_info(&d);
   if (st != FQ_OK) return st;
   const int64_t K8 = K / 8;
-  static int occ = 0;  // one wave
-  if (!occ) occ = resident_ctas(quant_mxfp8_kernel, 256, 0, 8);
-  const int grid = grid_for(R * K8, 256, d.sm_count, occ);
+  const int grid = wave_grid(quant_mxfp8_kernel, 256, R * K8, 256, d.sm_count, 8);
   return cuda_status(launch(quant_mxfp8_kernel, grid, 256, 0, reinterpret_cast<cudaStream_t>(stream), pdl_enabled(),
                             reinterpret_cast<const uint4*>(x), R, K8, reinterpret_cast<uint2*>(q), sf_blocked));
 }
