@@ -85,7 +85,8 @@ def lib():
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # an int: ctypes converts it for the c_void_p parameters
+    return None if t is None else t.data_ptr()
 
 
 _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
@@ -104,6 +105,8 @@ def _check(fn, status):
 
 
 def _cuda(t, dtype, name):
+    if isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dtype and t.is_contiguous():
+        return t
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
     if t.dtype != dtype:
@@ -144,6 +147,20 @@ def _workspace(nbytes, device, ws=None):
         cur = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         _WS[key] = cur
     return cur
+
+
+def _workspace_for(op, device, ws, a, b=0, c=0, d=0):
+    """The caller's workspace (uint8; the library checks its size and returns
+    FQ_ERR_WORKSPACE when it is too small), else a cached zero-filled one."""
+    if ws is not None:
+        return _cuda(ws, torch.uint8, "ws")
+    key = (device.index, op, a, b, c, d)
+    nb = _WS_BYTES.get(key)
+    if nb is None:
+        nb = int(lib().fq_workspace_bytes(op, a, b, c, d))
+        if nb:
+            _WS_BYTES[key] = nb
+    return _workspace(nb, device)
 
 
 def new_workspace(nbytes, device):
@@ -238,8 +255,7 @@ def mxfp8_linear(xq, xsf, wq, wsf, y=None, ws=None):
     M, K = xq.shape
     N = wq.shape[0]
     y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
-    nb = workspace_bytes(OP_MXFP8_LINEAR, M, K, N)
-    ws = _workspace(nb, xq.device, ws)
+    ws = _workspace_for(OP_MXFP8_LINEAR, xq.device, ws, M, K, N)
     _check("mxfp8_linear", lib().mxfp8_linear(_ptr(xq), _ptr(xsf), M, K, _ptr(wq), _ptr(wsf), N, _ptr(y), _ptr(ws),
                                               ws.numel() * ws.element_size(), _stream()))
     return y
@@ -264,8 +280,7 @@ def w8a8_linear(xq, sx, w_nk, sw, y=None, ws=None):
     M, K = xq.shape
     N = w_nk.shape[0]
     y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
-    nb = workspace_bytes(OP_W8A8_LINEAR, M, K, N)
-    ws = _workspace(nb, xq.device, ws)
+    ws = _workspace_for(OP_W8A8_LINEAR, xq.device, ws, M, K, N)
     _check("w8a8_linear", lib().w8a8_linear(_ptr(xq), _ptr(sx), M, K, _ptr(w_nk), _ptr(sw), N, _ptr(y),
                                             _ptr(ws), ws.numel(), _stream()))
     return y
@@ -280,8 +295,7 @@ def w8a8_quant_linear(x, w_nk, sw, y=None, return_quant=False, ws=None, xq=None,
     if return_quant:
         xq = torch.empty((M, K), dtype=torch.int8, device=x.device) if xq is None else xq
         sx = torch.empty((M,), dtype=torch.float32, device=x.device) if sx is None else sx
-    nb = workspace_bytes(OP_W8A8_QUANT_LINEAR, M, K, N)
-    ws = _workspace(nb, x.device, ws)
+    ws = _workspace_for(OP_W8A8_QUANT_LINEAR, x.device, ws, M, K, N)
     _check("w8a8_quant_linear", lib().w8a8_quant_linear(_ptr(x), M, K, _ptr(w_nk), _ptr(sw), N, _ptr(y), _ptr(xq),
                                                         _ptr(sx), _ptr(ws), ws.numel(), _stream()))
     return (y, xq, sx) if return_quant else y
@@ -349,8 +363,7 @@ def fp8_group_einsum(xq, sx, fmt, wq, sw_blk, y=None, ws=None):
     T, G, D = xq.shape
     N = wq.shape[1]
     y = torch.empty((T, G, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
-    nb = workspace_bytes(OP_FP8_GROUP_EINSUM, T, D, N, G)
-    ws = _workspace(nb, xq.device, ws)
+    ws = _workspace_for(OP_FP8_GROUP_EINSUM, xq.device, ws, T, D, N, G)
     _check("fp8_group_einsum", lib().fp8_group_einsum(_ptr(xq), _ptr(sx), fmt, T, G, D, _ptr(wq), _ptr(sw_blk), N,
                                                       _ptr(y), _ptr(ws), ws.numel(), _stream()))
     return y
@@ -394,8 +407,7 @@ def w8a8_grouped_linear(xq, sx, offsets, w_enk, sw_en, y=None, ws=None):
     R, K = xq.shape
     E, N, _ = w_enk.shape
     y = torch.empty((R, N), dtype=torch.bfloat16, device=xq.device) if y is None else y
-    nb = workspace_bytes(OP_W8A8_GROUPED_LINEAR, R, K, N, E)
-    ws = _workspace(nb, xq.device, ws)
+    ws = _workspace_for(OP_W8A8_GROUPED_LINEAR, xq.device, ws, R, K, N, E)
     _check("w8a8_grouped_linear", lib().w8a8_grouped_linear(_ptr(xq), _ptr(sx), _ptr(offsets), R, E, K, _ptr(w_enk),
                                                             _ptr(sw_en), N, _ptr(y), _ptr(ws), ws.numel(),
                                                             _stream()))
